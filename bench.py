@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one fused attention forward over the prefill workload
+(B=1, H=64, Nq=Nk=8192, d=128, BF16, no mask), the configuration the
+headline metric is quoted on. The same run also times, each with its own
+warm-up and timed loop, the causal workload (B=2, H=32, 8192^2, causal) and
+the split-KV decode workload (B=1, H=32, Nk=131072, d=128, 64 splits), and
+reports them as sub-objects. Rank 0 prints one JSON line.
+
+Inputs are larger than L2 (the prefill inputs are 384 MiB, decode K+V 2 GiB),
+so no L2 flush is done between iterations.
+
+For N > 1 (torchrun), every rank runs an independent replica of the
+workload on its own GPU (no collective on the data path: the problems are
+independent); a barrier and a max over ranks bracket the timed region and
+`value` counts the work of all ranks ("scaling": "weak").
+
+--impl reference times the FP64 CPU oracle (the reference implementation of
+this build) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from online_softmax_02_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s & % BF16 tcgen05 peak; split-KV decode HBM GB/s, % of peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch measured with ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the source file of the kernel and its
+# SHA-256 at capture time; reported as null when the source has changed.
+NCU_TRAFFIC = {
+    "fwd_sm103.cu": None,   # {"sha256": ..., "bytes_per_launch": ..., "workload": ...}
+    "decode.cu": None,
+}
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_sha(name):
+    path = os.path.join(ROOT, "online_softmax_02_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_for(name, units_scale=1.0):
+    rec = NCU_TRAFFIC.get(name)
+    if not rec or rec.get("sha256") != kernel_sha(name):
+        return None
+    return rec["bytes_per_launch"] * units_scale
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def visible_pairs(w: W.Workload, seqlens=None) -> int:
+    """Number of (query, key) pairs the mask leaves visible, summed over
+    batch and heads (closed form per row)."""
+    Nq, Nk = w.Nq, w.Nk
+    total = 0
+    for b in range(w.B):
+        L = Nk if seqlens is None else int(min(max(int(seqlens[b]), 0), Nk))
+        i = np.arange(Nq, dtype=np.int64)
+        hi = np.full(Nq, L, dtype=np.int64)                 # keys [lo, hi)
+        if w.mask_kind & (W.MASK_CAUSAL | W.MASK_WINDOW):
+            hi = np.minimum(hi, i + 1)
+        lo = np.zeros(Nq, dtype=np.int64)
+        if w.mask_kind & W.MASK_WINDOW:
+            lo = np.maximum(0, i - w.window + 1)
+        total += int(np.maximum(hi - lo, 0).sum())
+    return total * w.H
+
+
+def flops(w, seqlens=None):
+    """4 d FLOPs per visible pair: 2 d for q.k and 2 d for p v."""
+    return 4.0 * w.d * visible_pairs(w, seqlens)
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+        self.error = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError as e:
+            self.error = str(e)
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.error or not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": self.error or "no nvidia-smi samples"}
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0] and parts[0] not in self.uuid:
+                continue
+            rows.append(parts)
+        if not rows:
+            rows = [[p.strip() for p in ln.split(",")] for ln in self.lines if ln.count(",") >= 8]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s in sm if mx and s > 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def gpu_uuid(dev):
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        return "GPU-" + str(u)
+    except Exception:   # noqa: BLE001
+        return None
+
+
+# --------------------------------------------------------------- timing
+def time_loop(fn, steps, warmup, stream, dist_on):
+    """W warm-up calls, then K timed calls bracketed by barrier + sync;
+    returns (total ms on this rank via CUDA events, per-launch ms list)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    per = [a.elapsed_time(b) for a, b in evs]
+    return total, per
+
+
+def max_over_ranks(x, dist_on):
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args, rank, world, dist_on):
+    import online_softmax_02_gb300 as attn
+    attn.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    peaks, peak_src = load_peaks()
+
+    # ---------------- prefill (headline)
+    w = W.PREFILL
+    x = W.generate(w)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+
+    def step():
+        attn.attn_fwd(q, k, v, o=o, lse=lse, mask_kind=w.mask_kind, stream=stream)
+
+    with ClockSampler(gpu_uuid(dev)) as clk:
+        total_ms, per = time_loop(step, args.steps, args.warmup, stream, dist_on)
+    attn.attn_check_device_error(stream)
+    total_ms = max_over_ranks(total_ms, dist_on)
+    fl = flops(w)
+    ms_step = total_ms / args.steps
+    value = fl * world * args.steps / (total_ms * 1e-3) / 1e12
+    launch_ms = statistics.mean(per)
+    achieved = fl / (launch_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic_for("fwd_sm103.cu"),
+                "peak_source": "%s bf16_tflops (burst) from MEASURED_PEAKS.json" % peak_src
+                if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
+                "kernel": "fwd_sm103_kernel<128>",
+                "algorithmic_flops_per_launch": fl}
+
+    # ---------------- e2e through host buffers (pinned), same call
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            attn.attn_fwd(dq, dk, dv, o=o, lse=lse, mask_kind=w.mask_kind, stream=stream)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+    e_total, _ = time_loop(e2e_step, max(1, args.steps // 2), max(3, args.warmup // 2), stream,
+                           dist_on)
+    e_steps = max(1, args.steps // 2)
+    e_total = max_over_ranks(e_total, dist_on)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    e2e = {"value": round(fl * world * e_steps / (e_total * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(e_total / e_steps, 4)}
+
+    # ---------------- causal workload
+    wc = W.CAUSAL
+    xc = W.generate(wc)
+    qc, kc, vc = (xc[n].to(dev) for n in ("q", "k", "v"))
+    oc = torch.empty_like(qc)
+    lc = torch.empty(qc.shape[:3], dtype=torch.float32, device=dev)
+
+    def step_c():
+        attn.attn_fwd(qc, kc, vc, o=oc, lse=lc, mask_kind=wc.mask_kind, stream=stream)
+
+    c_total, c_per = time_loop(step_c, args.steps, args.warmup, stream, dist_on)
+    attn.attn_check_device_error(stream)
+    c_total = max_over_ranks(c_total, dist_on)
+    flc = flops(wc)
+    causal = {"config": wc.describe(), "ms_per_step": round(c_total / args.steps, 4),
+              "value": round(flc * world * args.steps / (c_total * 1e-3) / 1e12, 2),
+              "unit": "TFLOP/s", "flop_count": "causal (visible pairs only)",
+              "dense_equivalent_tflops": round(4.0 * wc.d * wc.B * wc.H * wc.Nq * wc.Nk * world *
+                                               args.steps / (c_total * 1e-3) / 1e12, 2),
+              "frac_of_peak": round(flc / (statistics.mean(c_per) * 1e-3) / 1e12 /
+                                    peaks["bf16_tflops"], 4)}
+    del qc, kc, vc, oc, lc, xc
+
+    # ---------------- split-KV decode
+    wd = W.DECODE
+    xd = W.generate(wd)
+    qd, kd, vd = (xd[n].to(dev) for n in ("q", "k", "v"))
+    od = torch.empty_like(qd)
+    ld = torch.empty((wd.B, wd.H, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(attn.attn_decode_workspace_bytes(wd.B, wd.H, wd.d, wd.num_splits),
+                     dtype=torch.uint8, device=dev)
+
+    def step_d():
+        attn.attn_decode_splitkv(qd, kd, vd, o=od, lse=ld, num_splits=wd.num_splits,
+                                 workspace=ws, stream=stream)
+
+    d_total, d_per = time_loop(step_d, args.steps, args.warmup, stream, dist_on)
+    attn.attn_check_device_error(stream)
+    d_total = max_over_ranks(d_total, dist_on)
+    kv_bytes = 2 * wd.B * wd.H * wd.Nk * wd.d * 2
+    alg_bytes = kv_bytes + 2 * wd.B * wd.H * wd.d * 2 + wd.B * wd.H * 4
+    d_ms = statistics.mean(d_per)
+    gbs = alg_bytes / (d_ms * 1e-3) / 1e9
+    decode = {"metric": "split-KV decode HBM GB/s", "config": wd.describe(),
+              "ms_per_step": round(d_total / args.steps, 4),
+              "value": round(alg_bytes * world * args.steps / (d_total * 1e-3) / 1e9, 1),
+              "unit": "GB/s", "gpu_launches_per_step": 2,
+              "workspace_bytes_per_step": int(2 * ws.numel()),
+              "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                           "traffic": traffic_for("decode.cu"),
+                           "algorithmic_bytes_per_step": alg_bytes,
+                           "note": "time is both launches (split + combine) per step"}}
+    del qd, kd, vd, xd
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), rounded to BF16)",
+        "config": dict(w.describe(), **{"parallelism": "replicas" if world > 1 else "single",
+                                        "l2": "inputs larger than L2 (384 MiB); no flush",
+                                        "flop_count": "4*d per visible (query, key) pair"}),
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+        "roofline": roofline,
+        "clocks": clk.summary(),
+        "causal": causal,
+        "decode": decode,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, x, o, args)
+    return result
+
+
+# ------------------------------------------------------ oracle on the host
+def oracle_sample(w, x, n_rows, seed=0):
+    import oracle
+    orc = oracle.Oracle()
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.B * w.H * w.Nq, size=n_rows, replace=False))
+    qn, kn, vn = (x[n].float().numpy() for n in ("q", "k", "v"))
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    ro, rl = orc.attention(qn, kn, vn, w.scale, w.mask_kind, w.window, None, rows=rows,
+                           threads=threads)
+    dt = time.perf_counter() - t0
+    return rows, ro, rl, dt, threads
+
+
+def cpu_baseline(w, x, o_gpu, args):
+    """The FP64 oracle, as it stands, on a bounded sample of rows of the
+    same workload, timed on the host cores; also reports its agreement with
+    the GPU output on those rows."""
+    # calibrate on a small sample, then size the sample to ~args.cpu_seconds
+    rows, _, _, dt, _ = oracle_sample(w, x, 64, seed=1)
+    n = int(min(w.B * w.H * w.Nq, max(64, 64 * args.cpu_seconds / max(dt, 1e-3))))
+    rows, ro, rl, dt, threads = oracle_sample(w, x, n, seed=2)
+    fl = 4.0 * w.d * w.Nk * n
+    got = o_gpu.float().reshape(-1, w.d)[torch.from_numpy(rows).to(o_gpu.device)].cpu().numpy()
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "%d random query rows (all %d keys each) of the prefill workload" % (n, w.Nk),
+            "max_abs_err_gpu_vs_oracle": float(np.abs(got - ro).max())}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step a bounded sample."""
+    w = W.PREFILL
+    x = W.generate(w)
+    _, _, _, dt0, _ = oracle_sample(w, x, 32, seed=1)
+    n = int(max(32, 32 * args.ref_seconds_per_step / max(dt0, 1e-3)))
+    for s in range(args.warmup):
+        oracle_sample(w, x, min(n, 64), seed=100 + s)
+    total = 0.0
+    threads = 1
+    for s in range(args.steps):
+        _, _, _, dt, threads = oracle_sample(w, x, n, seed=200 + s)
+        total += dt
+    fl = 4.0 * w.d * w.Nk * n
+    value = fl * args.steps / total / 1e12
+    return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(w.describe(), parallelism="host cores"), "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": "%d random query rows per step (all %d keys each)" % (n, w.Nk)},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds-per-step", type=float, default=6.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        args.steps = min(args.steps, 3)
+        print(json.dumps(run_reference(args, rank, world)))
+        return
+    dist_on = world > 1
+    if dist_on:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    try:
+        res = run_ours(args, rank, world, dist_on)
+        if rank == 0:
+            print(json.dumps(res))
+    finally:
+        if dist_on:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

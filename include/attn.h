@@ -1,0 +1,197 @@
+/*
+ * attn.h -- C interface of libattn.so: exact fused attention forward with
+ * online softmax, and split-KV decode, on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (all entry points):
+ *   For every batch b, head h and query row i, over the keys j visible
+ *   from i (mask below):
+ *     s_j   = scale * <q_i, k_j>
+ *     o_i   = sum_j softmax(s)_j v_j
+ *     lse_i = m + log(l), m = max_j s_j, l = sum_j exp(s_j - m)
+ *   Source pages:
+ *     P1 "Derive online softmax, prove it is exact, and explain why it makes
+ *        FlashAttention fast without reducing FLOPs"
+ *        (inferenceinterviews.com/q/online-softmax-derive-and-prove-flashattention):
+ *        "A strong answer" -- softmax attention for one query, the block
+ *        recurrence for (m, l, a), o = a / l exact; "What interviewers probe
+ *        next" -- the per-row log-sum-exp m + log l kept for the backward
+ *        pass, and split-KV (Flash-Decoding) for batch-1 long-context decode.
+ *     P2 "Implement online softmax for a whole tile of queries, not one
+ *        query, and write the rescaling step in matrix form"
+ *        (inferenceinterviews.com/q/online-softmax-query-tile-matrix-form):
+ *        "A strong answer" -- the query-tile equations S_j, m', P_j, l', A',
+ *        alpha and the single diag(l)^-1 at the end; the m_ref guard for rows
+ *        that see no key; causal masking by absolute position.
+ *     P3 "Online softmax" (interview.clozo.ai/blog/online-softmax.html):
+ *        "Step 4" -- the associative merge of partial results; "Trade-offs
+ *        and edge cases" -- Flash-Decoding's per-chunk log-sum-exp and final
+ *        rescaling reduction.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers, contiguous, row-major:
+ *     q [B,H,Nq,d], k and v [B,H,Nk,d], o [B,H,Nq,d], lse [B,H,Nq] (FP32,
+ *     natural log). Every tensor pointer must be 16-byte aligned.
+ *   - Masks (mask_kind, bit flags, combined by AND):
+ *       ATTN_MASK_CAUSAL  key j visible from query i iff j <= i (query i and
+ *                         key j at their own indices: top-left alignment).
+ *       ATTN_MASK_WINDOW  sliding window of `window` keys ending at the
+ *                         query: visible iff i - window < j <= i (implies the
+ *                         causal bound); window >= 1.
+ *       ATTN_MASK_PADDING keys j >= seqlens_k[b] invisible; seqlens_k is a
+ *                         device int32 [B] array, values clamped to [0, Nk].
+ *   - A row with no visible key gets o = 0 and lse = -inf (never NaN).
+ *   - Ownership: the caller allocates every buffer (including the decode
+ *     workspace); the library allocates no device memory on these paths and
+ *     keeps no state between calls except a per-device error word.
+ *   - Calls are asynchronous and stream-ordered on `stream` (0 = legacy
+ *     default stream). Argument errors are reported synchronously by the
+ *     return value, with a message in attn_last_error(); the outputs are then
+ *     untouched. A kernel whose bounded wait expired reports it through
+ *     attn_check_device_error().
+ *   - Supported head dims: d in {64, 128}; anything else is
+ *     ATTN_ERR_UNSUPPORTED.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or flag */
+    ATTN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d = 96)   */
+    ATTN_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed         */
+    ATTN_ERR_TIMEOUT = 4        /* a device-side bounded wait expired        */
+} attn_status_t;
+
+enum {
+    ATTN_MASK_NONE = 0,
+    ATTN_MASK_CAUSAL = 1,
+    ATTN_MASK_WINDOW = 2,
+    ATTN_MASK_PADDING = 4
+};
+
+/* Opaque CUDA stream handle (cudaStream_t / CUstream). */
+typedef void* attn_stream_t;
+
+/*
+ * attn_fwd -- fused attention forward, BF16 inputs and output.
+ *
+ * Computes o and lse as defined above for q, k, v in BF16 (o in BF16, lse in
+ * FP32). Query tiles of 128 rows stream 128-key blocks of K and V through
+ * shared memory; the running row max m, normalizer l and unnormalised
+ * accumulator A stay on chip (A in tensor memory), updated per block as
+ * A <- diag(alpha) A + P V with alpha = exp(m_old - m_new) (P2 "A strong
+ * answer"), with one diag(l)^-1 at the end; the score matrix never reaches
+ * device memory. P is rounded to BF16 for the P V product; m, l and A are
+ * FP32. Blocks that the mask hides entirely are skipped before they are
+ * loaded (P1 "Common mistakes", on causal masking).
+ *
+ *   q, k, v      device BF16 pointers, layout above.
+ *   o            device BF16 [B,H,Nq,d] (written).
+ *   lse          device FP32 [B,H,Nq] (written); may be NULL to skip it.
+ *   B, H         batch and heads, >= 0.
+ *   Nq, Nk       query and key lengths, >= 0 (Nk = 0: every row is empty).
+ *   d            head dimension, 64 or 128.
+ *   scale        score scale (usually 1/sqrt(d)); finite and > 0.
+ *   mask_kind    OR of ATTN_MASK_* flags.
+ *   window       window length (>= 1) when ATTN_MASK_WINDOW is set.
+ *   seqlens_k    device int32 [B], required iff ATTN_MASK_PADDING is set.
+ *   stream       CUDA stream.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v,
+                       void* o, float* lse,
+                       int B, int H, int Nq, int Nk, int d, float scale,
+                       int mask_kind, int window, const int* seqlens_k,
+                       attn_stream_t stream);
+
+/*
+ * attn_fwd_f32 -- the same operation with FP32 q, k, v and o (lse FP32).
+ * All arithmetic is FP32 on the CUDA cores; intended for accuracy checks of
+ * small problems such as P2's 1,000-key tile test. Arguments as attn_fwd.
+ */
+attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v,
+                           float* o, float* lse,
+                           int B, int H, int Nq, int Nk, int d, float scale,
+                           int mask_kind, int window, const int* seqlens_k,
+                           attn_stream_t stream);
+
+/*
+ * attn_decode_workspace_bytes -- size in bytes of the scratch buffer that
+ * attn_decode_splitkv needs for (B, H, d, num_splits): per (b, h, split) one
+ * FP32 partial output of d values and one FP32 partial log-sum-exp, at
+ * 256-byte-aligned offsets. Returns 0 for invalid arguments.
+ */
+size_t attn_decode_workspace_bytes(int B, int H, int d, int num_splits);
+
+/*
+ * attn_decode_splitkv -- split-KV decode (Flash-Decoding): one query row per
+ * (b, h), keys split into `num_splits` contiguous chunks of
+ * ceil(Nk / num_splits) keys.
+ *
+ * Launch 1 runs the online recurrence of P1 "A strong answer" over each
+ * chunk and writes the chunk's normalised output o_s and log-sum-exp lse_s
+ * to the workspace (an empty chunk writes o_s = 0, lse_s = -inf). Launch 2
+ * merges the chunks of each (b, h) with the rescaling rule of P3 "Step 4":
+ * m* = max_s lse_s, w_s = exp(lse_s - m*), o = sum_s w_s o_s / sum_s w_s,
+ * lse = m* + log(sum_s w_s).
+ *
+ *   q            device BF16 [B,H,1,d].
+ *   k, v         device BF16 [B,H,Nk,d].
+ *   o            device BF16 [B,H,1,d] (written).
+ *   lse          device FP32 [B,H,1] (written); may be NULL.
+ *   B, H, Nk, d  sizes (d in {64,128}); Nk >= 0.
+ *   scale        score scale; finite and > 0.
+ *   seqlens_k    device int32 [B] of visible key counts, or NULL for Nk.
+ *   num_splits   1 <= num_splits <= 1024.
+ *   workspace    device scratch of at least
+ *                attn_decode_workspace_bytes(B, H, d, num_splits) bytes,
+ *                256-byte aligned, owned by the caller; its contents are
+ *                overwritten. Two calls that share one workspace must be
+ *                ordered on the same stream.
+ *   workspace_bytes  its size.
+ *   stream       CUDA stream.
+ */
+attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v,
+                                  void* o, float* lse,
+                                  int B, int H, int Nk, int d, float scale,
+                                  const int* seqlens_k, int num_splits,
+                                  void* workspace, size_t workspace_bytes,
+                                  attn_stream_t stream);
+
+/*
+ * attn_check_device_error -- synchronise `stream`, then report whether any
+ * kernel of this library on the current device gave up a bounded wait since
+ * the last call (ATTN_ERR_TIMEOUT, and the error word is cleared), or
+ * whether the stream itself reported a CUDA error (ATTN_ERR_CUDA).
+ */
+attn_status_t attn_check_device_error(attn_stream_t stream);
+
+/*
+ * attn_selftest_bounded_wait -- diagnostic: launch one CTA that waits on a
+ * shared-memory barrier that nothing ever completes, with a limit of
+ * `limit_cycles` SM clock cycles (1 .. 2^31). The wait must give up, record
+ * the timeout in the error word and return, so that the following
+ * attn_check_device_error() reports ATTN_ERR_TIMEOUT and the context stays
+ * usable. Used by the tests of the failure path; faults nothing.
+ */
+attn_status_t attn_selftest_bounded_wait(long long limit_cycles,
+                                         attn_stream_t stream);
+
+/* attn_last_error -- message of the last failed call on this host thread
+ * ("" if none). The pointer stays valid until the next call on the thread. */
+const char* attn_last_error(void);
+
+/* attn_version -- library version string. */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

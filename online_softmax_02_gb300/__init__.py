@@ -1,0 +1,222 @@
+"""online_softmax_02_gb300 -- exact fused attention with online softmax on
+GB300 (sm_103a).
+
+A thin ctypes binding over ``libattn.so`` (C interface in ``include/attn.h``).
+This module only marshals arguments: every step of the computation runs in
+the library's CUDA kernels. PyTorch is used for device memory and streams.
+There is no CPU or PyTorch fallback: if the library is missing, ``load()``
+raises.
+
+Functions (same names as the C entry points):
+  attn_fwd(q, k, v, ...)            BF16 fused forward -> (o, lse)
+  attn_fwd_f32(q, k, v, ...)        FP32 fused forward -> (o, lse)
+  attn_decode_workspace_bytes(B, H, d, num_splits)
+  attn_decode_splitkv(q, k, v, ...) split-KV decode -> (o, lse)
+  attn_check_device_error(stream=None)
+  attn_selftest_bounded_wait(limit_cycles, stream=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from .workloads import MASK_CAUSAL, MASK_NONE, MASK_PADDING, MASK_WINDOW  # noqa: F401
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-OK status from libattn.so; `.status` holds the code."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__("attn status %d: %s" % (status, message))
+        self.status = status
+
+
+def load():
+    """Load libattn.so (built by ``__graft_entry__.build()`` or
+    ``online_softmax_02_gb300/build.py``). Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libattn.so not found at %s: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, P]
+    lib.attn_fwd.restype = I
+    lib.attn_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, P]
+    lib.attn_fwd_f32.restype = I
+    lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_decode_workspace_bytes.restype = S
+    lib.attn_decode_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, F, P, I, P, S, P]
+    lib.attn_decode_splitkv.restype = I
+    lib.attn_check_device_error.argtypes = [P]
+    lib.attn_check_device_error.restype = I
+    lib.attn_selftest_bounded_wait.argtypes = [ctypes.c_longlong, P]
+    lib.attn_selftest_bounded_wait.restype = I
+    lib.attn_last_error.argtypes = []
+    lib.attn_last_error.restype = ctypes.c_char_p
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != ATTN_OK:
+        raise AttnError(status, load().attn_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def _require(t, name, dtype, device=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def _fwd(fn, dtype, q, k, v, o, lse, scale, mask_kind, window, seqlens_k, stream):
+    import torch
+    _require(q, "q", dtype)
+    dev = q.device
+    _require(k, "k", dtype, dev)
+    _require(v, "v", dtype, dev)
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d] matching q")
+    if o is None:
+        o = torch.empty_like(q)
+    _require(o, "o", dtype, dev)
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape")
+    if lse is not None:
+        _require(lse, "lse", torch.float32, dev)
+        if tuple(lse.shape) != (B, H, Nq):
+            raise ValueError("lse must be [B, H, Nq]")
+    if seqlens_k is not None:
+        _require(seqlens_k, "seqlens_k", torch.int32, dev)
+        if tuple(seqlens_k.shape) != (B,):
+            raise ValueError("seqlens_k must be [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(dev):
+        st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                float(scale), int(mask_kind), int(window), _ptr(seqlens_k),
+                _stream_handle(stream, dev))
+    _check(st)
+    return o, lse
+
+
+def attn_fwd(q, k, v, o=None, lse=None, scale=None, mask_kind=MASK_NONE, window=0,
+             seqlens_k=None, stream=None, want_lse=True):
+    """BF16 fused attention forward through ``attn_fwd``.
+
+    q [B,H,Nq,d], k/v [B,H,Nk,d] contiguous BF16 CUDA tensors; returns
+    (o [B,H,Nq,d] BF16, lse [B,H,Nq] FP32 or None). Output buffers may be
+    passed in to avoid allocation."""
+    import torch
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    return _fwd(load().attn_fwd, torch.bfloat16, q, k, v, o, lse, scale, mask_kind,
+                window, seqlens_k, stream)
+
+
+def attn_fwd_f32(q, k, v, o=None, lse=None, scale=None, mask_kind=MASK_NONE, window=0,
+                 seqlens_k=None, stream=None, want_lse=True):
+    """FP32 fused attention forward through ``attn_fwd_f32``."""
+    import torch
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    return _fwd(load().attn_fwd_f32, torch.float32, q, k, v, o, lse, scale, mask_kind,
+                window, seqlens_k, stream)
+
+
+def attn_decode_workspace_bytes(B: int, H: int, d: int, num_splits: int) -> int:
+    return int(load().attn_decode_workspace_bytes(B, H, d, num_splits))
+
+
+def attn_decode_splitkv(q, k, v, o=None, lse=None, scale=None, seqlens_k=None,
+                        num_splits=64, workspace=None, stream=None, want_lse=True):
+    """Split-KV decode through ``attn_decode_splitkv``: q [B,H,1,d], k/v
+    [B,H,Nk,d] BF16. ``workspace``: a CUDA uint8 tensor of at least
+    ``attn_decode_workspace_bytes`` bytes (allocated here if None)."""
+    import torch
+    lib = load()
+    _require(q, "q", torch.bfloat16)
+    dev = q.device
+    _require(k, "k", torch.bfloat16, dev)
+    _require(v, "v", torch.bfloat16, dev)
+    if q.dim() != 4 or q.shape[2] != 1:
+        raise ValueError("q must be [B, H, 1, d]")
+    B, H, _, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d]")
+    if o is None:
+        o = torch.empty_like(q)
+    _require(o, "o", torch.bfloat16, dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _require(lse, "lse", torch.float32, dev)
+    if seqlens_k is not None:
+        _require(seqlens_k, "seqlens_k", torch.int32, dev)
+    need = int(lib.attn_decode_workspace_bytes(B, H, d, num_splits))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _require(workspace, "workspace", torch.uint8, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(dev):
+        st = lib.attn_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nk, d,
+                                     float(scale), _ptr(seqlens_k), int(num_splits),
+                                     _ptr(workspace), workspace.numel(),
+                                     _stream_handle(stream, dev))
+    _check(st)
+    return o, lse
+
+
+def attn_check_device_error(stream=None):
+    """Synchronise and raise AttnError if a kernel gave up a bounded wait."""
+    import torch
+    h = _stream_handle(stream, torch.cuda.current_device()) if stream is not None else None
+    _check(load().attn_check_device_error(h))
+
+
+def attn_selftest_bounded_wait(limit_cycles: int, stream=None):
+    import torch
+    h = _stream_handle(stream, torch.cuda.current_device()) if stream is not None else None
+    _check(load().attn_selftest_bounded_wait(int(limit_cycles), h))
+
+
+def attn_version() -> str:
+    return load().attn_version().decode()

@@ -1,0 +1,288 @@
+// attn_api.cu -- the C interface of libattn.so (declared in include/attn.h):
+// argument checks, TMA tensor-map encoding, launch, the per-device error
+// word, and the small utility kernels (empty-row fill, bounded-wait
+// self-test).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/attn.h"
+#include "common.cuh"
+
+#define ATTN_API extern "C" __attribute__((visibility("default")))
+
+namespace attn {
+
+cudaError_t launch_fwd_sm103_maps(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, cudaStream_t stream);
+
+namespace {
+
+__device__ unsigned int g_err_word = 0;   // see WaitSite in common.cuh
+
+thread_local std::string t_last_error;
+
+attn_status_t fail(attn_status_t st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+attn_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device address of the error word on the current device (cached per device).
+attn_status_t err_word(unsigned int** out) {
+    static std::mutex mu;
+    static unsigned int* cache[128] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 128) return fail(ATTN_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_err_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        cache[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = cache[dev];
+    return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D BF16 tensor map over [B*H][rows][d] with a 64 x 128 x 1 box and
+// 128-byte swizzle (one swizzle atom row = 64 BF16 head dims).
+attn_status_t encode_bf16_3d(CUtensorMap* m, const void* ptr, int d, int rows, long long bh) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(bh)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return ATTN_OK;
+}
+
+__global__ void fill_empty_kernel(void* o, float* lse, long long rows, int d, int is_bf16) {
+    const long long n = rows * d;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        if (is_bf16) static_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16_rn(0.f);
+        else static_cast<float*>(o)[i] = 0.f;
+        if (lse != nullptr && i % d == 0) lse[i / d] = -INFINITY;
+    }
+}
+
+__global__ void selftest_wait_kernel(unsigned int* err, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on `bar`: the wait must give up after `limit`.
+    wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, err, kSiteSelftest, limit);
+}
+
+// Checks shared by attn_fwd and attn_fwd_f32. Returns ATTN_OK and sets
+// *empty when there is nothing to compute.
+attn_status_t check_fwd(const void* q, const void* k, const void* v, const void* o, int B, int H,
+                        int Nq, int Nk, int d, float scale, int mask_kind, int window,
+                        const int* seqlens_k, bool* nothing) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d Nq=%d Nk=%d)", B, H, Nq, Nk);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW | ATTN_MASK_PADDING))
+        return fail(ATTN_ERR_INVALID_ARG, "unknown mask bits 0x%x", mask_kind);
+    if ((mask_kind & ATTN_MASK_WINDOW) && window < 1)
+        return fail(ATTN_ERR_INVALID_ARG, "window must be >= 1 with ATTN_MASK_WINDOW");
+    if (((mask_kind & ATTN_MASK_PADDING) != 0) != (seqlens_k != nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "seqlens_k must be given iff ATTN_MASK_PADDING is set");
+    if (B > 65535 || H > 65535)
+        return fail(ATTN_ERR_UNSUPPORTED, "B and H must be <= 65535");
+    *nothing = (static_cast<long long>(B) * H * Nq == 0);
+    if (*nothing) return ATTN_OK;
+    if (q == nullptr || o == nullptr) return fail(ATTN_ERR_INVALID_ARG, "q and o must not be NULL");
+    if (Nk > 0 && (k == nullptr || v == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "k and v must not be NULL");
+    if (!aligned16(q) || !aligned16(o) || (Nk > 0 && (!aligned16(k) || !aligned16(v))))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int Nq, int Nk, int d, float scale, int mask_kind,
+                                int window, const int* seqlens_k, attn_stream_t stream) {
+    bool nothing = false;
+    attn_status_t st = check_fwd(q, k, v, o, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k,
+                                 &nothing);
+    if (st != ATTN_OK || nothing) return st;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long rows = static_cast<long long>(B) * H * Nq;
+    if (Nk == 0) {
+        cudaError_t e = launch_fill_empty(o, lse, rows, d, true, s);
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fill kernel launch");
+    }
+    unsigned int* err = nullptr;
+    if ((st = err_word(&err)) != ATTN_OK) return st;
+    CUtensorMap tq, tk, tv;
+    const long long bh = static_cast<long long>(B) * H;
+    if ((st = encode_bf16_3d(&tq, q, d, Nq, bh)) != ATTN_OK) return st;
+    if ((st = encode_bf16_3d(&tk, k, d, Nk, bh)) != ATTN_OK) return st;
+    if ((st = encode_bf16_3d(&tv, v, d, Nk, bh)) != ATTN_OK) return st;
+    FwdArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k, err};
+    cudaError_t e = launch_fwd_sm103_maps(a, tq, tk, tv, s);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd kernel launch");
+}
+
+ATTN_API attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v, float* o,
+                                    float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                                    int mask_kind, int window, const int* seqlens_k,
+                                    attn_stream_t stream) {
+    bool nothing = false;
+    attn_status_t st = check_fwd(q, k, v, o, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k,
+                                 &nothing);
+    if (st != ATTN_OK || nothing) return st;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long rows = static_cast<long long>(B) * H * Nq;
+    cudaError_t e;
+    if (Nk == 0) {
+        e = launch_fill_empty(o, lse, rows, d, false, s);
+    } else {
+        FwdArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k, nullptr};
+        e = launch_fwd_f32(a, s);
+    }
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd_f32 kernel launch");
+}
+
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+}
+
+ATTN_API size_t attn_decode_workspace_bytes(int B, int H, int d, int num_splits) {
+    if (B < 0 || H < 0 || d <= 0 || num_splits < 1 || num_splits > 1024) return 0;
+    const size_t slots = static_cast<size_t>(B) * H * num_splits;
+    return align256(slots * d * sizeof(float)) + align256(slots * sizeof(float));
+}
+
+ATTN_API attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v, void* o,
+                                           float* lse, int B, int H, int Nk, int d, float scale,
+                                           const int* seqlens_k, int num_splits, void* workspace,
+                                           size_t workspace_bytes, attn_stream_t stream) {
+    if (B < 0 || H < 0 || Nk < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d Nk=%d)", B, H, Nk);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (num_splits < 1 || num_splits > 1024)
+        return fail(ATTN_ERR_INVALID_ARG, "num_splits=%d outside [1, 1024]", num_splits);
+    if (B > 65535 || H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B and H must be <= 65535");
+    if (static_cast<long long>(B) * H == 0) return ATTN_OK;
+    if (q == nullptr || o == nullptr) return fail(ATTN_ERR_INVALID_ARG, "q and o must not be NULL");
+    if (Nk > 0 && (k == nullptr || v == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "k and v must not be NULL");
+    if (!aligned16(q) || !aligned16(o) || (Nk > 0 && (!aligned16(k) || !aligned16(v))))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    const size_t need = attn_decode_workspace_bytes(B, H, d, num_splits);
+    if (workspace == nullptr || workspace_bytes < need)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
+                    workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t slots = static_cast<size_t>(B) * H * num_splits;
+    float* ws_o = static_cast<float*>(workspace);
+    float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             align256(slots * d * sizeof(float)));
+    DecodeArgs a{q, k, v, o, lse, B, H, Nk, d, scale, seqlens_k, num_splits, ws_o, ws_lse, nullptr};
+    cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_splitkv kernel launch");
+}
+
+ATTN_API attn_status_t attn_check_device_error(attn_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int* word = nullptr;
+    attn_status_t st = err_word(&word);
+    if (st != ATTN_OK) return st;
+    unsigned int w = 0;
+    e = cudaMemcpy(&w, word, sizeof(w), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read error word");
+    if (w != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+        return fail(ATTN_ERR_TIMEOUT, "device wait gave up (site %u)", w >> 8);
+    }
+    return ATTN_OK;
+}
+
+ATTN_API attn_status_t attn_selftest_bounded_wait(long long limit_cycles, attn_stream_t stream) {
+    if (limit_cycles < 1 || limit_cycles > (1LL << 31))
+        return fail(ATTN_ERR_INVALID_ARG, "limit_cycles outside [1, 2^31]");
+    unsigned int* err = nullptr;
+    attn_status_t st = err_word(&err);
+    if (st != ATTN_OK) return st;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, limit_cycles);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "selftest kernel launch");
+}
+
+ATTN_API const char* attn_last_error(void) { return t_last_error.c_str(); }
+
+ATTN_API const char* attn_version(void) { return "online_softmax_02_gb300 0.1.0 (sm_103a)"; }
+
+namespace attn {
+cudaError_t launch_fill_empty(void* o, float* lse, long long rows, int d, bool bf16,
+                              cudaStream_t stream) {
+    const long long n = rows * d;
+    const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 4096));
+    fill_empty_kernel<<<blocks, 256, 0, stream>>>(o, lse, rows, d, bf16 ? 1 : 0);
+    return cudaGetLastError();
+}
+}  // namespace attn

@@ -1,0 +1,87 @@
+// common.cuh -- pieces shared by the kernels of libattn.so: the device error
+// word protocol, bounded mbarrier waits, BF16 helpers and the internal
+// launcher declarations.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include "ptx.cuh"
+
+namespace attn {
+
+// Mask bits (same values as ATTN_MASK_* in include/attn.h).
+constexpr int kMaskCausal = 1;
+constexpr int kMaskWindow = 2;
+constexpr int kMaskPadding = 4;
+
+// Device error word: 0 = no error. A bounded wait that gives up stores
+// (site << 8) | 1 with atomicCAS, so the first site that timed out is kept.
+enum WaitSite : uint32_t {
+    kSiteQFull = 1, kSiteKFull, kSiteVFull, kSiteKEmpty, kSiteVEmpty,
+    kSiteSFull, kSitePFull, kSiteODone, kSiteDrain, kSiteSelftest
+};
+
+// Default limit of one wait, in SM clock cycles (about a second at the
+// clocks these parts run at). Legitimate waits inside one CTA are
+// microseconds long.
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+// Wait until the phase of `bar` with parity `parity` completes. Gives up
+// (returns false) when `*abort_flag` is set by another role of the CTA, or
+// after `limit` cycles, in which case it records the site in the error word
+// and raises the CTA's abort flag so that the other roles stop too.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, unsigned int* err,
+                                             uint32_t site, long long limit = kWaitLimitCycles) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            *abort_flag = 1;
+            atomicCAS(err, 0u, (site << 8) | 1u);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// Exact widening of BF16 to FP32 (the BF16 bits are the high half).
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Arguments common to the forward launchers.
+struct FwdArgs {
+    const void* q; const void* k; const void* v;
+    void* o; float* lse;
+    int B, H, Nq, Nk, d;
+    float scale;
+    int mask_kind, window;
+    const int* seqlens_k;
+    unsigned int* err;     // device error word
+};
+
+// Internal launchers (return a cudaError_t from the launch; argument checks
+// happen in attn_api.cu before these are called).
+cudaError_t launch_fwd_f32(const FwdArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+    const void* q; const void* k; const void* v;
+    void* o; float* lse;
+    int B, H, Nk, d;
+    float scale;
+    const int* seqlens_k;
+    int num_splits;
+    float* ws_o;       // [B,H,num_splits,d]
+    float* ws_lse;     // [B,H,num_splits]
+    unsigned int* err;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_fill_empty(void* o, float* lse, long long rows, int d, bool bf16,
+                              cudaStream_t stream);
+
+}  // namespace attn

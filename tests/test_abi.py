@@ -1,0 +1,123 @@
+"""The C interface without a GPU: libattn.so loads, exports every function
+include/attn.h declares, and rejects bad arguments synchronously (these
+calls return before any CUDA call, so no device is needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from online_softmax_02_gb300 import build
+    build.build()
+    import online_softmax_02_gb300 as attn
+    return attn.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ["attn_fwd", "attn_fwd_f32", "attn_decode_splitkv",
+                 "attn_decode_workspace_bytes", "attn_check_device_error",
+                 "attn_last_error"]:
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from online_softmax_02_gb300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (attn_\w+)", out))
+    declared = set(declared_functions())
+    assert declared <= exported, declared - exported
+    # nothing else with the attn_ prefix leaks out
+    assert exported == declared, exported - declared
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def test_constants_match_header():
+    import online_softmax_02_gb300 as attn
+    from online_softmax_02_gb300 import workloads as W
+    text = open(HEADER).read()
+    vals = dict((k, int(v)) for k, v in re.findall(r"(ATTN_\w+)\s*=\s*(\d+)", text))
+    assert vals["ATTN_OK"] == attn.ATTN_OK == 0
+    assert vals["ATTN_ERR_INVALID_ARG"] == attn.ATTN_ERR_INVALID_ARG
+    assert vals["ATTN_ERR_UNSUPPORTED"] == attn.ATTN_ERR_UNSUPPORTED
+    assert vals["ATTN_ERR_CUDA"] == attn.ATTN_ERR_CUDA
+    assert vals["ATTN_ERR_TIMEOUT"] == attn.ATTN_ERR_TIMEOUT
+    assert vals["ATTN_MASK_CAUSAL"] == W.MASK_CAUSAL
+    assert vals["ATTN_MASK_WINDOW"] == W.MASK_WINDOW
+    assert vals["ATTN_MASK_PADDING"] == W.MASK_PADDING
+
+
+def test_version_and_workspace_size(lib):
+    assert b"sm_103a" in lib.attn_version()
+    # 1*32*64 slots: 2048*128 floats + 2048 floats, each padded to 256 bytes
+    assert lib.attn_decode_workspace_bytes(1, 32, 128, 64) == 2048 * 128 * 4 + 2048 * 4
+    assert lib.attn_decode_workspace_bytes(1, 1, 64, 3) == 768 + 256
+    assert lib.attn_decode_workspace_bytes(1, 1, 64, 5) == 1280 + 256
+    assert lib.attn_decode_workspace_bytes(1, 1, 64, 0) == 0
+    assert lib.attn_decode_workspace_bytes(1, 1, 64, 1025) == 0
+
+
+FAKE = 0x10000   # never dereferenced: every case below fails validation first
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), 2),
+    (dict(d=64, B=-1), 1),
+    (dict(scale=0.0), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(mask_kind=8), 1),
+    (dict(mask_kind=2, window=0), 1),
+    (dict(mask_kind=4, seqlens=None), 1),
+    (dict(mask_kind=0, seqlens=FAKE), 1),
+    (dict(q=FAKE + 8), 1),
+    (dict(o=0), 1),
+    (dict(H=70000), 2),
+])
+def test_forward_argument_errors(lib, kw, code):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, H=2, Nq=16, Nk=16, d=128,
+             scale=0.125, mask_kind=0, window=0, seqlens=None)
+    a.update(kw)
+    for fn in (lib.attn_fwd, lib.attn_fwd_f32):
+        st = fn(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"],
+                a["d"], a["scale"], a["mask_kind"], a["window"], a["seqlens"], None)
+        assert st == code
+        assert lib.attn_last_error() != b""
+
+
+def test_forward_empty_problem_is_ok(lib):
+    assert lib.attn_fwd(None, None, None, None, None, 0, 4, 16, 16, 128, 0.1, 0, 0, None, None) == 0
+    assert lib.attn_fwd(None, None, None, None, None, 1, 4, 0, 16, 64, 0.1, 0, 0, None, None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=32), 2),
+    (dict(num_splits=0), 1),
+    (dict(num_splits=2000), 1),
+    (dict(ws=None), 1),
+    (dict(ws_bytes=10), 1),
+    (dict(ws=FAKE + 16), 1),
+    (dict(k=FAKE + 4), 1),
+])
+def test_decode_argument_errors(lib, kw, code):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, H=2, Nk=100, d=128, scale=0.1,
+             seqlens=None, num_splits=4, ws=FAKE, ws_bytes=1 << 20)
+    a.update(kw)
+    st = lib.attn_decode_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                                 a["Nk"], a["d"], a["scale"], a["seqlens"], a["num_splits"],
+                                 a["ws"], a["ws_bytes"], None)
+    assert st == code

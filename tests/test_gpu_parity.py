@@ -1,0 +1,289 @@
+"""CUDA path against the FP64 oracle, element by element, through the C
+interface (GPU only).
+
+Tolerances (from the accuracy targets of this library):
+  BF16 forward / decode: max |o - o_ref| <= 2e-2, max |lse - lse_ref| <= 1e-3.
+  FP32 forward: max |o - o_ref| / max |o_ref| <= 1e-5 (normwise relative),
+                max |lse - lse_ref| <= 1e-5.
+  Always: no NaN; lse is -inf exactly where the oracle's is (rows with no
+  visible key), and o is exactly 0 there.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from online_softmax_02_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_O_BF16, TOL_LSE = 2e-2, 1e-3
+TOL_O_F32_REL, TOL_LSE_F32 = 1e-5, 1e-5
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy()
+
+
+def assert_close(o, lse, ro, rl, tol_o, tol_l, rel=False, what=""):
+    o = np.asarray(o, np.float64)
+    lse = np.asarray(lse, np.float64)
+    assert not np.isnan(o).any(), (what, "NaN in o")
+    assert not np.isnan(lse).any(), (what, "NaN in lse")
+    empty = np.isneginf(rl)
+    assert np.array_equal(np.isneginf(lse), empty), (what, "lse -inf pattern differs")
+    assert np.isfinite(lse[~empty]).all(), (what, "inf in lse")
+    if empty.any():
+        assert np.all(o[empty] == 0.0), (what, "empty rows must be 0")
+    err_o = np.abs(o - ro).max() if o.size else 0.0
+    if rel:
+        err_o = err_o / max(np.abs(ro).max(), 1e-30)
+    err_l = np.abs(lse[~empty] - rl[~empty]).max() if (~empty).any() else 0.0
+    assert err_o <= tol_o, (what, "o error", err_o)
+    assert err_l <= tol_l, (what, "lse error", err_l)
+    return err_o, err_l
+
+
+def run_fwd(attn, x, mask_kind=0, window=0, scale=None, dtype=torch.bfloat16):
+    dev = torch.device("cuda:0")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    sl = x.get("seqlens_k")
+    sl = sl.to(dev) if sl is not None else None
+    fn = attn.attn_fwd if dtype == torch.bfloat16 else attn.attn_fwd_f32
+    o, lse = fn(q, k, v, scale=scale, mask_kind=mask_kind, window=window, seqlens_k=sl)
+    attn.attn_check_device_error()
+    return _np(o), _np(lse)
+
+
+def oracle_fwd(orc, x, mask_kind=0, window=0, scale=None, rows=None):
+    d = x["q"].shape[-1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    sl = x.get("seqlens_k")
+    return orc.attention(_np(x["q"]), _np(x["k"]), _np(x["v"]), scale, mask_kind, window,
+                         None if sl is None else sl.numpy(), rows=rows)
+
+
+# --------------------------------------------------------------- FP32 path
+@pytest.mark.parametrize("q0", [0, 300, 872])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("planted", [False, True])
+def test_tile_test_fp32(cuda_lib, orc, q0, causal, planted):
+    """P2's test: 128 query rows at tile offset q0 over 1,000 keys, d = 64."""
+    w = W.tile_test(q0, causal, planted)
+    x = W.generate(w)
+    o, lse = run_fwd(cuda_lib, x, w.mask_kind, dtype=torch.float32)
+    ro, rl = oracle_fwd(orc, x, w.mask_kind)
+    assert_close(o, lse, ro, rl, TOL_O_F32_REL, TOL_LSE_F32, rel=True, what=w.name)
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 2, 300, 300, 128, 0, 0), (2, 1, 257, 1000, 64, W.MASK_CAUSAL, 0),
+    (1, 3, 100, 100, 128, W.MASK_WINDOW, 7), (2, 2, 65, 129, 64, W.MASK_PADDING, 0),
+])
+def test_fwd_f32_shapes(cuda_lib, orc, shape):
+    B, H, Nq, Nk, d, mk, win = shape
+    x = W.random_inputs(B, H, Nq, Nk, d, dtype=torch.float32, seed=11,
+                        seqlen_range=(0, Nk) if mk & W.MASK_PADDING else None)
+    o, lse = run_fwd(cuda_lib, x, mk, win, dtype=torch.float32)
+    ro, rl = oracle_fwd(orc, x, mk, win)
+    assert_close(o, lse, ro, rl, TOL_O_F32_REL, TOL_LSE_F32, rel=True, what=str(shape))
+
+
+# ------------------------------------------------------ BF16 tensor-core path
+FWD_SHAPES = [
+    # B, H, Nq, Nk, d, mask, window, seqlen_range
+    (1, 2, 256, 256, 128, 0, 0, None),            # one CTA, exact tiles
+    (1, 2, 300, 300, 128, 0, 0, None),            # ragged query and key tails
+    (2, 3, 513, 700, 128, W.MASK_CAUSAL, 0, None),
+    (1, 2, 1000, 1000, 64, 0, 0, None),
+    (1, 2, 1000, 1000, 64, W.MASK_CAUSAL, 0, None),
+    (1, 1, 5, 3, 128, 0, 0, None),                # smaller than a tile
+    (1, 1, 1, 1, 128, W.MASK_CAUSAL, 0, None),
+    (1, 2, 100, 1000, 128, W.MASK_CAUSAL, 0, None),   # Nq < Nk, top-left causal
+    (1, 2, 1000, 100, 128, W.MASK_CAUSAL, 0, None),   # Nq > Nk
+    (2, 2, 777, 777, 128, W.MASK_WINDOW, 200, None),
+    (3, 2, 600, 600, 128, W.MASK_WINDOW | W.MASK_PADDING, 64, (0, 600)),
+    (4, 1, 515, 515, 64, W.MASK_PADDING, 0, (0, 515)),
+    (2, 2, 300, 300, 128, W.MASK_WINDOW | W.MASK_PADDING, 1, (1, 300)),
+    (2, 2, 640, 640, 128, W.MASK_CAUSAL | W.MASK_PADDING, 0, (50, 640)),
+]
+
+
+@pytest.mark.parametrize("shape", FWD_SHAPES, ids=[str(s) for s in FWD_SHAPES])
+def test_fwd_bf16_shapes(cuda_lib, orc, shape):
+    B, H, Nq, Nk, d, mk, win, sr = shape
+    x = W.random_inputs(B, H, Nq, Nk, d, seed=hash(shape) % 1000, seqlen_range=sr)
+    o, lse = run_fwd(cuda_lib, x, mk, win)
+    ro, rl = oracle_fwd(orc, x, mk, win)
+    assert_close(o, lse, ro, rl, TOL_O_BF16, TOL_LSE, what=str(shape))
+
+
+def test_fwd_bf16_large_scores(cuda_lib, orc):
+    """Scores of magnitude ~100: the running max must keep exp in range."""
+    x = W.random_inputs(1, 2, 400, 700, 128, seed=5, scale_q=30.0)
+    o, lse = run_fwd(cuda_lib, x, W.MASK_CAUSAL)
+    ro, rl = oracle_fwd(orc, x, W.MASK_CAUSAL)
+    assert_close(o, lse, ro, rl, TOL_O_BF16, 5e-3 if np.abs(rl).max() > 100 else TOL_LSE,
+                 what="large scores")
+
+
+def test_fwd_bf16_late_max(cuda_lib, orc):
+    """Largest scores planted in the last five keys (the max arrives late)."""
+    x = W.random_inputs(1, 2, 256, 1000, 128, seed=6)
+    x["q"][..., -1] = 1.0
+    x["k"][:, :, -5:, -1] += 10.0 * math.sqrt(128)
+    o, lse = run_fwd(cuda_lib, x)
+    ro, rl = oracle_fwd(orc, x)
+    assert_close(o, lse, ro, rl, TOL_O_BF16, TOL_LSE, what="late max")
+
+
+def test_fwd_bf16_no_keys(cuda_lib, orc):
+    """Nk = 0 and all-zero seqlens: every row empty."""
+    x = W.random_inputs(1, 2, 130, 0, 128, seed=7)
+    o, lse = run_fwd(cuda_lib, x)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+    x = W.random_inputs(2, 2, 130, 260, 128, seed=8)
+    x["seqlens_k"] = torch.zeros(2, dtype=torch.int32)
+    o, lse = run_fwd(cuda_lib, x, W.MASK_PADDING)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+def test_fwd_bf16_lse_optional(cuda_lib, orc):
+    x = W.random_inputs(1, 1, 200, 200, 128, seed=9)
+    dev = torch.device("cuda:0")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o, lse = cuda_lib.attn_fwd(q, k, v, want_lse=False)
+    assert lse is None
+    ro, _ = oracle_fwd(orc, x)
+    assert np.abs(_np(o) - ro).max() <= TOL_O_BF16
+
+
+# ---------------------------------------- full-size workloads, sampled rows
+def _sample_rows(B, H, Nq, n, seed):
+    rng = np.random.default_rng(seed)
+    fixed = []
+    for bh in (0, B * H - 1):
+        for i in (0, 1, 127, 128, 255, 256, Nq // 2, Nq - 129, Nq - 128, Nq - 1):
+            if 0 <= i < Nq:
+                fixed.append(bh * Nq + i)
+    rand = rng.choice(B * H * Nq, size=n, replace=False)
+    return np.unique(np.concatenate([np.array(fixed, np.int64), rand.astype(np.int64)]))
+
+
+@pytest.mark.parametrize("wname", ["PREFILL", "CAUSAL", "MASKED"])
+def test_full_size_workloads(cuda_lib, orc, wname):
+    """The benchmarked workloads at full size, in the benchmark's launch
+    configuration: sampled rows against the oracle one by one, and
+    properties over every row (no NaN, empty rows exactly 0 / -inf)."""
+    w = getattr(W, wname)
+    x = W.generate(w)
+    o, lse = run_fwd(cuda_lib, x, w.mask_kind, w.window)
+    rows = _sample_rows(w.B, w.H, w.Nq, 384, seed=1)
+    ro, rl = oracle_fwd(orc, x, w.mask_kind, w.window, rows=rows)
+    o_flat = o.reshape(-1, w.d)[rows]
+    lse_flat = lse.reshape(-1)[rows]
+    assert_close(o_flat, lse_flat, ro, rl, TOL_O_BF16, TOL_LSE, what=w.name)
+    assert not np.isnan(o).any() and not np.isnan(lse).any()
+    if w.mask_kind & W.MASK_PADDING:
+        # row i of batch b sees no key iff i >= L_b + window - 1
+        L = x["seqlens_k"].numpy()
+        i = np.arange(w.Nq)
+        for b in range(w.B):
+            empty = i >= L[b] + w.window - 1
+            assert np.all(np.isneginf(lse[b][:, empty]))
+            assert np.all(o[b][:, empty] == 0)
+            assert np.all(np.isfinite(lse[b][:, ~empty]))
+
+
+# ------------------------------------------------------------ split-KV decode
+def run_decode(attn, x, num_splits, scale=None, with_ws=False):
+    dev = torch.device("cuda:0")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    sl = x.get("seqlens_k")
+    sl = sl.to(dev) if sl is not None else None
+    B, H, _, d = q.shape
+    ws = torch.empty(attn.attn_decode_workspace_bytes(B, H, d, num_splits), dtype=torch.uint8,
+                     device=dev)
+    o, lse = attn.attn_decode_splitkv(q, k, v, scale=scale, seqlens_k=sl, num_splits=num_splits,
+                                      workspace=ws)
+    attn.attn_check_device_error()
+    if with_ws:
+        return _np(o), _np(lse), ws
+    return _np(o), _np(lse)
+
+
+def test_decode_full_size(cuda_lib, orc):
+    w = W.DECODE
+    x = W.generate(w)
+    o, lse = run_decode(cuda_lib, x, w.num_splits)
+    ro, rl = oracle_fwd(orc, x)
+    assert_close(o, lse, ro, rl, TOL_O_BF16, TOL_LSE, what=w.name)
+
+
+DECODE_SHAPES = [
+    # B, H, Nk, d, splits, seqlen_range
+    (1, 4, 1000, 128, 8, None),
+    (2, 3, 777, 64, 5, None),
+    (1, 2, 100, 128, 64, None),          # more splits than 2-key chunks: empty splits
+    (3, 2, 4096, 128, 16, (0, 4096)),    # padded, including empty sequences
+    (1, 1, 1, 128, 1, None),
+    (2, 2, 5000, 128, 1, None),
+]
+
+
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=[str(s) for s in DECODE_SHAPES])
+def test_decode_shapes(cuda_lib, orc, shape):
+    B, H, Nk, d, S, sr = shape
+    x = W.random_inputs(B, H, 1, Nk, d, seed=Nk % 97, seqlen_range=sr)
+    o, lse = run_decode(cuda_lib, x, S)
+    mk = W.MASK_PADDING if sr else 0
+    ro, rl = oracle_fwd(orc, x, mk)
+    assert_close(o, lse, ro, rl, TOL_O_BF16, TOL_LSE, what=str(shape))
+
+
+def test_decode_split_partials(cuda_lib, orc):
+    """The workspace holds, per (b, h, split), the chunk's normalised output
+    and log-sum-exp: compare each with the oracle on that chunk's keys."""
+    B, H, Nk, d, S = 1, 2, 1000, 128, 7
+    x = W.random_inputs(B, H, 1, Nk, d, seed=21)
+    _, _, ws = run_decode(cuda_lib, x, S, with_ws=True)
+    slots = B * H * S
+    wso = ws[: slots * d * 4].view(torch.float32).reshape(B, H, S, d).cpu().numpy()
+    off = ((slots * d * 4 + 255) // 256) * 256
+    wsl = ws[off: off + slots * 4].view(torch.float32).reshape(B, H, S).cpu().numpy()
+    chunk = -(-Nk // S)
+    for s in range(S):
+        a, b = s * chunk, min((s + 1) * chunk, Nk)
+        y = {"q": x["q"], "k": x["k"][:, :, a:b].contiguous(), "v": x["v"][:, :, a:b].contiguous()}
+        ro, rl = oracle_fwd(orc, y)
+        assert np.abs(wso[:, :, s] - ro[:, :, 0]).max() <= 1e-3
+        assert np.abs(wsl[:, :, s] - rl[:, :, 0]).max() <= 1e-4
+
+
+# ------------------------------------------------------------ failure path
+def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib, orc):
+    """A wait on a barrier nothing completes gives up after its limit, the
+    error surfaces as ATTN_ERR_TIMEOUT, and the next call still works."""
+    cuda_lib.attn_selftest_bounded_wait(2_000_000)
+    with pytest.raises(cuda_lib.AttnError) as ei:
+        cuda_lib.attn_check_device_error()
+    assert ei.value.status == cuda_lib.ATTN_ERR_TIMEOUT
+    cuda_lib.attn_check_device_error()          # cleared
+    x = W.random_inputs(1, 1, 130, 130, 128, seed=3)
+    o, lse = run_fwd(cuda_lib, x)
+    ro, rl = oracle_fwd(orc, x)
+    assert_close(o, lse, ro, rl, TOL_O_BF16, TOL_LSE)
+
+
+def test_bad_arguments_raise(cuda_lib):
+    dev = torch.device("cuda:0")
+    q = torch.zeros(1, 1, 16, 96, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(cuda_lib.AttnError) as ei:
+        cuda_lib.attn_fwd(q, q, q)
+    assert ei.value.status == cuda_lib.ATTN_ERR_UNSUPPORTED
+    buf = torch.zeros(1 + 16 * 128, dtype=torch.bfloat16, device=dev)
+    qm = buf[1:].view(1, 1, 16, 128)             # 2-byte offset: misaligned
+    with pytest.raises(cuda_lib.AttnError) as ei:
+        cuda_lib.attn_fwd(qm, qm, qm)
+    assert ei.value.status == cuda_lib.ATTN_ERR_INVALID_ARG
