@@ -24,6 +24,7 @@ this build) on a bounded sample of the same workload, on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -227,8 +228,13 @@ def run_ours(args, rank, world, dist_on):
     stream = torch.cuda.Stream(dev)
     peaks, peak_src = load_peaks()
 
+    result = {}
     # ---------------- prefill (headline)
     w = W.PREFILL
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads, name="%s_H%d" % (w.name, args.heads))
+    if args.only not in ("all", "prefill"):
+        return run_sections(args, rank, world, dist_on, dev, stream, peaks, result)
     x = W.generate(w)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     o = torch.empty_like(q)
@@ -280,6 +286,30 @@ def run_ours(args, rank, world, dist_on):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": round(e_total / e_steps, 4)}
 
+    result.update({
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1), rounded to BF16)",
+        "config": dict(w.describe(), **{"parallelism": "replicas" if world > 1 else "single",
+                                        "l2": "inputs larger than L2 (384 MiB); no flush",
+                                        "flop_count": "4*d per visible (query, key) pair"}),
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+        "roofline": roofline,
+        "clocks": clk.summary(),
+    })
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, x, o, args)
+    del q, k, v, o, lse, dq, dk, dv, x
+    return run_sections(args, rank, world, dist_on, dev, stream, peaks, result)
+
+
+def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
+    """The causal and split-KV decode workloads (sub-objects of the line)."""
+    import online_softmax_02_gb300 as attn
+    if args.only not in ("all", "causal"):
+        return run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result)
     # ---------------- causal workload
     wc = W.CAUSAL
     xc = W.generate(wc)
@@ -302,9 +332,18 @@ def run_ours(args, rank, world, dist_on):
               "frac_of_peak": round(flc / (statistics.mean(c_per) * 1e-3) / 1e12 /
                                     peaks["bf16_tflops"], 4)}
     del qc, kc, vc, oc, lc, xc
+    result["causal"] = causal
+    return run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result)
 
+
+def run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result):
+    import online_softmax_02_gb300 as attn
+    if args.only not in ("all", "decode"):
+        return result
     # ---------------- split-KV decode
     wd = W.DECODE
+    if args.decode_nk:
+        wd = dataclasses.replace(wd, Nk=args.decode_nk, name="%s_Nk%d" % (wd.name, args.decode_nk))
     xd = W.generate(wd)
     qd, kd, vd = (xd[n].to(dev) for n in ("q", "k", "v"))
     od = torch.empty_like(qd)
@@ -334,24 +373,7 @@ def run_ours(args, rank, world, dist_on):
                            "algorithmic_bytes_per_step": alg_bytes,
                            "note": "time is both launches (split + combine) per step"}}
     del qd, kd, vd, xd
-
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded N(0,1), rounded to BF16)",
-        "config": dict(w.describe(), **{"parallelism": "replicas" if world > 1 else "single",
-                                        "l2": "inputs larger than L2 (384 MiB); no flush",
-                                        "flop_count": "4*d per visible (query, key) pair"}),
-        "gpu_launches": args.steps,
-        "e2e": e2e,
-        "roofline": roofline,
-        "clocks": clk.summary(),
-        "causal": causal,
-        "decode": decode,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, x, o, args)
+    result["decode"] = decode
     return result
 
 
@@ -422,6 +444,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds-per-step", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # profiling helpers: run one section, or a reduced size of it
+    ap.add_argument("--only", choices=["all", "prefill", "causal", "decode"], default="all")
+    ap.add_argument("--heads", type=int, default=0, help="override H of the prefill workload")
+    ap.add_argument("--decode-nk", type=int, default=0, help="override Nk of the decode workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
