@@ -165,6 +165,35 @@ attn_status_t attn_decode_splitkv(const void* q, const void* k, const void* v,
                                   attn_stream_t stream);
 
 /*
+ * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot
+ * allocate device memory on their call path (for example a serving process
+ * whose device memory is all reserved for its own pool, or one that must not
+ * call cudaMalloc/cudaFree there because those calls can synchronise the
+ * device). The source pages have no counterpart to this entry point: it only
+ * changes where the per-split partials are kept.
+ *
+ * Same arguments, layout and result as attn_decode_splitkv, without the
+ * workspace: the partials go to a fixed 4 MiB array inside the library
+ * (allocated by the CUDA loader, held on every GPU that loads the library
+ * until the process exits). The call allocates nothing.
+ *   - Limit: attn_decode_workspace_bytes(B, H, d, num_splits) must be at most
+ *     4 MiB (4194304 bytes); larger problems return ATTN_ERR_INVALID_ARG with
+ *     a message, and need attn_decode_splitkv with a caller workspace.
+ *   - The first call on a device looks up the array's device address on
+ *     that device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents (no part of it needs to start at zero). Calls whose
+ *     kernels overlap on the GPU, e.g. on two unordered streams, race on it:
+ *     order them on one stream.
+ */
+attn_status_t attn_decode_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                          void* o, float* lse,
+                                          int B, int H, int Nk, int d, float scale,
+                                          const int* seqlens_k, int num_splits,
+                                          attn_stream_t stream);
+
+/*
  * attn_check_device_error -- synchronise `stream`, then report whether any
  * kernel of this library on the current device gave up a bounded wait since
  * the last call (ATTN_ERR_TIMEOUT, and the error word is cleared), or

@@ -12,6 +12,7 @@ Functions (same names as the C entry points):
   attn_fwd_f32(q, k, v, ...)        FP32 fused forward -> (o, lse)
   attn_decode_workspace_bytes(B, H, d, num_splits)
   attn_decode_splitkv(q, k, v, ...) split-KV decode -> (o, lse)
+  attn_decode_splitkv_noalloc(q, k, v, o, ...)  the same, no caller workspace
   attn_check_device_error(stream=None)
   attn_selftest_bounded_wait(limit_cycles, stream=None)
 """
@@ -61,6 +62,8 @@ def load():
     lib.attn_decode_workspace_bytes.restype = S
     lib.attn_decode_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, F, P, I, P, S, P]
     lib.attn_decode_splitkv.restype = I
+    lib.attn_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, F, P, I, P]
+    lib.attn_decode_splitkv_noalloc.restype = I
     lib.attn_check_device_error.argtypes = [P]
     lib.attn_check_device_error.restype = I
     lib.attn_selftest_bounded_wait.argtypes = [ctypes.c_longlong, P]
@@ -201,6 +204,44 @@ def attn_decode_splitkv(q, k, v, o=None, lse=None, scale=None, seqlens_k=None,
                                      float(scale), _ptr(seqlens_k), int(num_splits),
                                      _ptr(workspace), workspace.numel(),
                                      _stream_handle(stream, dev))
+    _check(st)
+    return o, lse
+
+
+def attn_decode_splitkv_noalloc(q, k, v, o, lse=None, scale=None, seqlens_k=None,
+                                num_splits=64, stream=None):
+    """Split-KV decode through ``attn_decode_splitkv_noalloc``: the same result
+    as ``attn_decode_splitkv`` for callers that cannot allocate device memory
+    on their call path. The C entry point allocates nothing; its per-split
+    partials live in a fixed 4 MiB array inside libattn.so, shared by every
+    call on a device (calls that overlap on the GPU race on it). The output
+    buffers ``o`` (and ``lse`` if wanted) must be passed in. Problems whose
+    partials need more than 4 MiB raise AttnError (ATTN_ERR_INVALID_ARG)."""
+    import torch
+    lib = load()
+    _require(q, "q", torch.bfloat16)
+    dev = q.device
+    _require(k, "k", torch.bfloat16, dev)
+    _require(v, "v", torch.bfloat16, dev)
+    if q.dim() != 4 or q.shape[2] != 1:
+        raise ValueError("q must be [B, H, 1, d]")
+    B, H, _, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d]")
+    _require(o, "o", torch.bfloat16, dev)
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape")
+    if lse is not None:
+        _require(lse, "lse", torch.float32, dev)
+    if seqlens_k is not None:
+        _require(seqlens_k, "seqlens_k", torch.int32, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(dev):
+        st = lib.attn_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                             Nk, d, float(scale), _ptr(seqlens_k),
+                                             int(num_splits), _stream_handle(stream, dev))
     _check(st)
     return o, lse
 

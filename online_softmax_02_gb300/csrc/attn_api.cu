@@ -244,6 +244,45 @@ ATTN_API attn_status_t attn_decode_splitkv(const void* q, const void* k, const v
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_splitkv kernel launch");
 }
 
+ATTN_API attn_status_t attn_decode_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                                   void* o, float* lse, int B, int H, int Nk,
+                                                   int d, float scale, const int* seqlens_k,
+                                                   int num_splits, attn_stream_t stream) {
+    if (B < 0 || H < 0 || Nk < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d Nk=%d)", B, H, Nk);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (num_splits < 1 || num_splits > 1024)
+        return fail(ATTN_ERR_INVALID_ARG, "num_splits=%d outside [1, 1024]", num_splits);
+    if (B > 65535 || H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B and H must be <= 65535");
+    if (static_cast<long long>(B) * H == 0) return ATTN_OK;
+    if (q == nullptr || o == nullptr) return fail(ATTN_ERR_INVALID_ARG, "q and o must not be NULL");
+    if (Nk > 0 && (k == nullptr || v == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "k and v must not be NULL");
+    if (!aligned16(q) || !aligned16(o) || (Nk > 0 && (!aligned16(k) || !aligned16(v))))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    const size_t need = attn_decode_workspace_bytes(B, H, d, num_splits);
+    void* scratch = nullptr;
+    size_t have = 0;
+    cudaError_t e = decode_static_scratch(&scratch, &have);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+    if (need > have)
+        return fail(ATTN_ERR_INVALID_ARG,
+                    "attn_decode_splitkv_noalloc: B*H*num_splits*(d+1) partials need %zu bytes, "
+                    "more than the fixed %zu-byte scratch; use attn_decode_splitkv with a workspace",
+                    need, have);
+    const size_t slots = static_cast<size_t>(B) * H * num_splits;
+    float* ws_o = static_cast<float*>(scratch);
+    float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                             align256(slots * d * sizeof(float)));
+    DecodeArgs a{q, k, v, o, lse, B, H, Nk, d, scale, seqlens_k, num_splits, ws_o, ws_lse, nullptr};
+    e = launch_decode(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_splitkv_noalloc kernel launch");
+}
+
 ATTN_API attn_status_t attn_check_device_error(attn_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

@@ -81,6 +81,9 @@ struct DecodeArgs {
     unsigned int* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// Device address and size of decode.cu's fixed scratch array on the current
+// device (looked up on first use per device).
+cudaError_t decode_static_scratch(void** ptr, size_t* bytes);
 cudaError_t launch_fill_empty(void* o, float* lse, long long rows, int d, bool bf16,
                               cudaStream_t stream);
 

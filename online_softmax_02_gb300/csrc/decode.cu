@@ -19,6 +19,8 @@
 // the output: the split kernel is bound by HBM bandwidth. Each warp streams
 // its keys with 16-byte non-allocating loads, 16 keys (d = 128) per batch,
 // so every lane has 16 independent loads in flight per batch.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace attn {
@@ -240,6 +242,54 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
                                                                a.num_splits);
     }
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Decode without caller-provided scratch.
+//
+// Some callers cannot hand this library a device buffer for the split
+// partials: a serving process that has reserved all device memory for its own
+// pool and forbids allocation on the request path, or a caller that must not
+// call cudaMalloc/cudaFree there because those calls can synchronise the
+// device and stall work on other streams. For them the split partials live in
+// the fixed array below instead of a workspace argument.
+//
+// Limits and sharing:
+//   * kStaticScratchBytes (4 MiB) is the whole array; it holds the partials
+//     of B * H * num_splits (b, h, split) slots: d FP32 outputs per slot plus
+//     one FP32 log-sum-exp per slot, laid out exactly like the workspace of
+//     attn_decode_splitkv (attn_decode_workspace_bytes). Problems that need
+//     more are rejected.
+//   * Every GPU that loads libattn.so holds this array until the process exits.
+//   * All calls on a device share the one array and it keeps the last call's
+//     contents. Nothing in it has to start at zero: the split launch writes
+//     every slot the combine launch then reads. Two calls whose kernels
+//     overlap on the GPU (for example on two streams without ordering between
+//     them) race on the array and give wrong results.
+//   * In host code the name g_decode_scratch is only a host-side stand-in for
+//     the device array; its device address is looked up once per device with
+//     cudaGetSymbolAddress (below), with that device current.
+// ---------------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+cudaError_t decode_static_scratch(void** ptr, size_t* bytes) {
+    static std::mutex mu;
+    static void* cache[128] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        cache[dev] = p;
+    }
+    *ptr = cache[dev];
+    *bytes = kStaticScratchBytes;
+    return cudaSuccess;
 }
 
 }  // namespace attn
