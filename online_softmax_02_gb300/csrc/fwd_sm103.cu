@@ -12,27 +12,39 @@
 // and O_i = diag(l)^-1 A once after the last block; lse = m + log l
 // (P1 "Derive online softmax, prove it is exact, ...", "What interviewers
 // probe next"). Blocks that the mask hides entirely are never loaded (P1
-// "Common mistakes", on causal masking). The rescale of A is skipped for a
-// warp whose 32 rows all kept their max (alpha is then exactly 1; P2 "What
-// interviewers probe next").
+// "Common mistakes", on causal masking).
 //
-// GB300 mapping (one CTA per SM, 320 threads):
+// Rescaling. P2 ("What interviewers probe next") notes that alpha is exactly 1
+// when the max does not change, and that the FlashAttention-4 variant goes
+// further: it moves the reference only when the max grows past a threshold,
+// which stays exact because l and A share the reference and the final
+// division cancels it. This kernel does the latter: each row keeps a
+// reference m_use that moves to the block max only when that exceeds m_use by
+// more than kTau = 8 (log2 units), so P <= 2^8, and A is rescaled in tensor
+// memory only for warps where some row moved; lse = m_use + log l.
+//
+// GB300 mapping (one CTA per SM, 352 threads):
 //   * Two query tiles per CTA (256 rows) share every K/V block, so each
 //     block is read from device memory once per 256 queries, and the tensor
 //     core works on one tile's products while the other tile's softmax runs.
-//   * Warp 8 issues TMA bulk-tensor loads: Q once, then K_j and V_j into a
-//     2-stage ring of 128-byte-swizzled shared-memory buffers, tracked by
-//     mbarriers with transaction counts.
+//   * Warp 8 issues TMA bulk-tensor loads of Q (once) and streams K_j into a
+//     3-slot ring; warp 10 streams V_j into a 2-slot ring (5 and 5 at
+//     d = 64); 128-byte-swizzled shared-memory buffers tracked by mbarriers
+//     with transaction counts.
 //   * Warp 9 allocates 512 tensor-memory columns (S_0, S_1, O_0, O_1; FP32)
-//     and one lane issues every tcgen05.mma: S_t = Q_t K_j^T with both
+//     and runs the MMA schedule as a whole warp (uniform control flow, so the
+//     loop state and operand descriptors stay in uniform registers); one
+//     lane elected with elect.sync issues every tcgen05.mma: S_t = Q_t K_j^T with both
 //     operands in shared memory, and O_t += P_t V_j with P_t read from tensor
 //     memory (BF16, written over S_t) and V_j from shared memory. Issue order
 //     per block: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j).
 //   * Warps 0-3 run the softmax of tile 0 and warps 4-7 that of tile 1, one
 //     thread per query row: tcgen05.ld of the 128 scores of its row, mask,
-//     row max and row sum in registers (no shuffles: the row is in one
-//     thread), exp2 with the scale folded into one FMA, P stored back to
-//     tensor memory, A rescaled in tensor memory when a row's max moved, then
+//     row max (four independent three-input max chains) and row sum (packed
+//     FP32x2 adds) in registers -- no shuffles, the row is in one thread --,
+//     exp2 with the scale folded into one packed FMA, P stored back to tensor
+//     memory in two 64-key halves, each signalled separately so the PV
+//     product of the first half runs while the second half is computed; then
 //     the epilogue O = A / l and lse.
 //   * m, l and A are FP32; P is rounded to BF16 for the P V product.
 //   * Every mbarrier wait is bounded; on expiry the CTA records the site in
@@ -48,16 +60,23 @@ constexpr int BM = 128;                 // query rows per tile
 constexpr int NT = 2;                   // query tiles per CTA
 constexpr int BN = 128;                 // keys per block
 constexpr int kSoftmaxWarps = 4 * NT;
-constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kProducerWarp = kSoftmaxWarps;       // Q and K loads
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kProducerVWarp = kSoftmaxWarps + 2;  // V loads
+constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Lazy-rescale threshold in log2 units: the row's reference max moves only
+// when a block's max exceeds it by more than this (P stays <= 2^kTau = 256).
+constexpr float kTau = 8.0f;
 
 template <int D>
 struct Cfg {
-    static constexpr int kStages = (D == 64) ? 4 : 2;
+    // K/V ring depths: K is consumed one MMA step ahead of V, so it gets the
+    // deeper ring (Q 64 KiB + K 3 x 32 KiB + V 2 x 32 KiB = 224 KiB at d = 128).
+    static constexpr int kStagesK = (D == 64) ? 5 : 3;
+    static constexpr int kStagesV = (D == 64) ? 5 : 2;
     static constexpr uint32_t kRowBytes = 128;                 // one swizzle atom row
     static constexpr uint32_t kQTileBytes = BM * D * 2;
     static constexpr uint32_t kKVBytes = BN * D * 2;
@@ -65,21 +84,22 @@ struct Cfg {
     static constexpr uint32_t kKVChunkBytes = BN * kRowBytes;  // 64 head dims of a K/V block
     static constexpr uint32_t kQOff = 0;
     static constexpr uint32_t kKOff = kQOff + NT * kQTileBytes;
-    static constexpr uint32_t kVOff = kKOff + kStages * kKVBytes;
-    static constexpr uint32_t kBarOff = kVOff + kStages * kKVBytes;
+    static constexpr uint32_t kVOff = kKOff + kStagesK * kKVBytes;
+    static constexpr uint32_t kBarOff = kVOff + kStagesV * kKVBytes;
     // barrier indices
     static constexpr int bQFull = 0;
     static constexpr int bKFull = 1;
-    static constexpr int bKEmpty = bKFull + kStages;
-    static constexpr int bVFull = bKEmpty + kStages;
-    static constexpr int bVEmpty = bVFull + kStages;
-    static constexpr int bSFull = bVEmpty + kStages;
-    static constexpr int bPFull = bSFull + NT;
-    static constexpr int bODone = bPFull + NT;
+    static constexpr int bKEmpty = bKFull + kStagesK;
+    static constexpr int bVFull = bKEmpty + kStagesK;
+    static constexpr int bVEmpty = bVFull + kStagesV;
+    static constexpr int bSFull = bVEmpty + kStagesV;
+    static constexpr int bPFull = bSFull + NT;         // [NT][2]: per tile, per key half
+    static constexpr int bODone = bPFull + 2 * NT;
     static constexpr int bDrain = bODone + NT;
     static constexpr int kNumBars = bDrain + 1;
     static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
     static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
     static constexpr uint32_t s_col(int t) { return t * BN; }
     static constexpr uint32_t o_col(int t) { return NT * BN + t * D; }
     static_assert(NT * BN + NT * D <= kTmemCols, "tensor memory budget");
@@ -118,7 +138,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  int window, const int* __restrict__ seqlens_k, unsigned int* __restrict__ err,
                  int reverse_order) {
     using C = Cfg<D>;
-    constexpr int NS = C::kStages;
+    constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -149,15 +169,18 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(C::bQFull), 1);
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NSK; ++s) {
             ptx::mbar_init(bar(C::bKFull + s), 1);
             ptx::mbar_init(bar(C::bKEmpty + s), 1);
+        }
+        for (int s = 0; s < NSV; ++s) {
             ptx::mbar_init(bar(C::bVFull + s), 1);
             ptx::mbar_init(bar(C::bVEmpty + s), 1);
         }
         for (int t = 0; t < NT; ++t) {
             ptx::mbar_init(bar(C::bSFull + t), 1);
-            ptx::mbar_init(bar(C::bPFull + t), 4);   // one arrival per softmax warp
+            ptx::mbar_init(bar(C::bPFull + 2 * t), 4);       // one arrival per softmax warp
+            ptx::mbar_init(bar(C::bPFull + 2 * t + 1), 4);
             ptx::mbar_init(bar(C::bODone + t), 1);
         }
         ptx::mbar_init(bar(C::bDrain), 1);
@@ -173,126 +196,180 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0 && lo < hi) {
-            ptx::prefetch_tmap(&tm_q);
-            ptx::prefetch_tmap(&tm_k);
-            ptx::prefetch_tmap(&tm_v);
-            ptx::mbar_arrive_expect_tx(bar(C::bQFull), NT * C::kQTileBytes);
-            for (int t = 0; t < NT; ++t)
-                for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d(sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes,
-                                     &tm_q, bar(C::bQFull), c * 64, q0 + t * BM, bh);
+    if (warp == kProducerWarp || warp == kProducerVWarp) {
+        // ------------------------------------------------------ TMA producers
+        // Warp 8 loads Q and streams K; warp 10 streams V. Each ring is
+        // refilled as soon as the MMA warp releases a slot. The whole warp
+        // runs the loop (uniform control flow); one elected lane issues.
+        if (lo < hi) {
+            const bool leader = ptx::elect_one();
+            const bool is_k = (warp == kProducerWarp);
+            const int ns = is_k ? NSK : NSV;
+            const int full0 = is_k ? C::bKFull : C::bVFull;
+            const int empty0 = is_k ? C::bKEmpty : C::bVEmpty;
+            const uint32_t ring = sbase + (is_k ? C::kKOff : C::kVOff);
+            const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+            if (leader) {
+                ptx::prefetch_tmap(map);
+                if (is_k) {
+                    ptx::prefetch_tmap(&tm_q);
+                    ptx::mbar_arrive_expect_tx(bar(C::bQFull), NT * C::kQTileBytes);
+                    for (int t = 0; t < NT; ++t)
+                        for (int c = 0; c < D / 64; ++c)
+                            ptx::tma_load_3d(sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes,
+                                             &tm_q, bar(C::bQFull), c * 64, q0 + t * BM, bh);
+                }
+            }
             int issued = 0;
             for (int s = lo; s < hi; ++s) {
-                const int i = s - lo, st = i % NS;
-                const uint32_t ph = (i / NS) & 1;
-                if (!wait_bounded(bar(C::bKEmpty + st), ph ^ 1, abort_flag, err, kSiteKEmpty)) break;
-                ptx::mbar_arrive_expect_tx(bar(C::bKFull + st), C::kKVBytes);
-                for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d(sbase + C::kKOff + st * C::kKVBytes + c * C::kKVChunkBytes,
-                                     &tm_k, bar(C::bKFull + st), c * 64, s * BN, bh);
-                if (!wait_bounded(bar(C::bVEmpty + st), ph ^ 1, abort_flag, err, kSiteVEmpty)) {
-                    issued = 2 * i + 1;
-                    break;
+                const int i = s - lo, st = i % ns;
+                const uint32_t ph = (i / ns) & 1;
+                const bool got = wait_bounded(bar(empty0 + st), ph ^ 1, abort_flag, err,
+                                              is_k ? kSiteKEmpty : kSiteVEmpty);
+                if (!__all_sync(0xffffffffu, got)) break;
+                if (leader) {
+                    ptx::mbar_arrive_expect_tx(bar(full0 + st), C::kKVBytes);
+                    for (int c = 0; c < D / 64; ++c)
+                        ptx::tma_load_3d(ring + st * C::kKVBytes + c * C::kKVChunkBytes, map,
+                                         bar(full0 + st), c * 64, s * BN, bh);
                 }
-                ptx::mbar_arrive_expect_tx(bar(C::bVFull + st), C::kKVBytes);
-                for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_load_3d(sbase + C::kVOff + st * C::kKVBytes + c * C::kKVChunkBytes,
-                                     &tm_v, bar(C::bVFull + st), c * 64, s * BN, bh);
-                issued = 2 * (i + 1);
+                __syncwarp();
+                issued = i + 1;
             }
-            if (*abort_flag) {
-                // Let the copies this thread started land before the CTA exits.
-                wait_bounded(bar(C::bQFull), 0, nullptr, err, kSiteDrain, kWaitLimitCycles / 8);
-                for (int n = max(0, issued - 2 * NS); n < issued; ++n) {
-                    const int i = n / 2, st = i % NS;
-                    const uint32_t ph = (i / NS) & 1;
-                    wait_bounded(bar(((n & 1) ? C::bVFull : C::bKFull) + st), ph, nullptr, err,
-                                 kSiteDrain, kWaitLimitCycles / 8);
-                }
+            if (*abort_flag && leader) {
+                // Let the copies this warp started land before the CTA exits.
+                if (is_k)
+                    wait_bounded(bar(C::bQFull), 0, nullptr, err, kSiteDrain, kWaitLimitCycles / 8);
+                for (int i = max(0, issued - ns); i < issued; ++i)
+                    wait_bounded(bar(full0 + i % ns), (i / ns) & 1, nullptr, err, kSiteDrain,
+                                 kWaitLimitCycles / 8);
             }
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0 && lo < hi) {
+        // The whole warp runs the schedule and waits; one elected lane issues
+        // every tcgen05.mma / tcgen05.commit, so the loop state and the
+        // operand descriptors stay warp-uniform.
+        if (lo < hi) {
+            const bool leader = ptx::elect_one();
             constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(BM, D, true);
             int p_seen[NT], pv_done[NT];
 #pragma unroll
             for (int t = 0; t < NT; ++t) { p_seen[t] = 0; pv_done[t] = 0; }
-            bool ok = wait_bounded(bar(C::bQFull), 0, abort_flag, err, kSiteQFull);
+            bool ok = __all_sync(0xffffffffu,
+                                 wait_bounded(bar(C::bQFull), 0, abort_flag, err, kSiteQFull));
             for (int s = lo; ok && s <= hi; ++s) {
-                const int i = s - lo, st = i % NS;
-                const uint32_t ph = (i / NS) & 1;
-                const int pst = (i + NS - 1) % NS;
-                const uint32_t pph = ((i - 1) / NS) & 1;
-                if (s - 1 >= lo) {
-                    ok = wait_bounded(bar(C::bVFull + pst), pph, abort_flag, err, kSiteVFull);
-                    if (!ok) break;
-                }
-                if (s < hi) {
-                    ok = wait_bounded(bar(C::bKFull + st), ph, abort_flag, err, kSiteKFull);
-                    if (!ok) break;
-                }
-                ptx::tc_fence_after();
+                const int i = s - lo;
+                const int kst = i % NSK;                       // K slot of block s
+                const uint32_t kph = (i / NSK) & 1;
+                const int vst = (i + NSV - 1) % NSV;           // V slot of block s - 1
+                const uint32_t vph = ((i - 1) / NSV) & 1;
+                // Full barriers are waited right before their first use, and
+                // every block's barriers are waited once per step.
+                bool k_ready = !(s < hi), v_ready = !(s - 1 >= lo);
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (s - 1 >= R[t].lo && s - 1 < R[t].hi) {
-                        // O_t (+)= P_t V_{s-1}
-                        ok = wait_bounded(bar(C::bPFull + t), p_seen[t] & 1, abort_flag, err,
-                                          kSitePFull);
+                        // O_t (+)= P_t V_{s-1}, one 64-key half at a time as the
+                        // softmax hands each half of P over.
+                        if (!v_ready) {
+                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bVFull + vst), vph,
+                                                                      abort_flag, err, kSiteVFull));
+                            if (!ok) break;
+                            v_ready = true;
+                        }
+                        const uint32_t vbase = sbase + C::kVOff + vst * C::kKVBytes;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            ok = __all_sync(0xffffffffu,
+                                            wait_bounded(bar(C::bPFull + 2 * t + half), p_seen[t] & 1,
+                                                         abort_flag, err, kSitePFull));
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            if (leader) {
+#pragma unroll
+                                for (int k4 = 0; k4 < BN / 32; ++k4) {
+                                    const int kk = half * (BN / 32) + k4;
+                                    const uint64_t bdesc = ptx::sdesc_sw128(
+                                        vbase + kk * 16 * C::kRowBytes, C::kKVChunkBytes, 1024);
+                                    ptx::mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
+                                                bdesc, kIdescPV,
+                                                (pv_done[t] > 0 || kk > 0) ? 1u : 0u);
+                                }
+                            }
+                            __syncwarp();
+                        }
                         if (!ok) break;
                         ++p_seen[t];
-                        ptx::tc_fence_after();
-                        const uint32_t vbase = sbase + C::kVOff + pst * C::kKVBytes;
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            const uint64_t bdesc =
-                                ptx::sdesc_sw128(vbase + kk * 16 * C::kRowBytes, C::kKVChunkBytes, 1024);
-                            ptx::mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, bdesc,
-                                        kIdescPV, (pv_done[t] > 0 || kk > 0) ? 1u : 0u);
-                        }
                         ++pv_done[t];
-                        if (s - 1 == R[t].hi - 1) ptx::mma_commit(bar(C::bODone + t));
+                        if (s - 1 == R[t].hi - 1 && leader) ptx::mma_commit(bar(C::bODone + t));
+                        __syncwarp();
                     }
                     if (s < hi && s >= R[t].lo && s < R[t].hi) {
                         // S_t = Q_t K_s^T
-                        const uint32_t qbase = sbase + C::kQOff + t * C::kQTileBytes;
-                        const uint32_t kbase = sbase + C::kKOff + st * C::kKVBytes;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t koff = (kk / 4) * C::kQChunkBytes + (kk % 4) * 32;
-                            const uint32_t boff = (kk / 4) * C::kKVChunkBytes + (kk % 4) * 32;
-                            const uint64_t adesc = ptx::sdesc_sw128(qbase + koff, 16, 1024);
-                            const uint64_t bdesc = ptx::sdesc_sw128(kbase + boff, 16, 1024);
-                            ptx::mma_ss(tmem + C::s_col(t), adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
+                        if (!k_ready) {
+                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKFull + kst), kph,
+                                                                      abort_flag, err, kSiteKFull));
+                            if (!ok) break;
+                            ptx::tc_fence_after();
+                            k_ready = true;
                         }
-                        ptx::mma_commit(bar(C::bSFull + t));
+                        const uint32_t qbase = sbase + C::kQOff + t * C::kQTileBytes;
+                        const uint32_t kbase = sbase + C::kKOff + kst * C::kKVBytes;
+                        if (leader) {
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t koff = (kk / 4) * C::kQChunkBytes + (kk % 4) * 32;
+                                const uint32_t boff = (kk / 4) * C::kKVChunkBytes + (kk % 4) * 32;
+                                const uint64_t adesc = ptx::sdesc_sw128(qbase + koff, 16, 1024);
+                                const uint64_t bdesc = ptx::sdesc_sw128(kbase + boff, 16, 1024);
+                                ptx::mma_ss(tmem + C::s_col(t), adesc, bdesc, kIdescS,
+                                            kk > 0 ? 1u : 0u);
+                            }
+                            ptx::mma_commit(bar(C::bSFull + t));
+                        }
+                        __syncwarp();
                     }
                 }
                 if (!ok) break;
-                if (s - 1 >= lo) ptx::mma_commit(bar(C::bVEmpty + pst));
-                if (s < hi) ptx::mma_commit(bar(C::bKEmpty + st));
+                if (!v_ready)
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bVFull + vst), vph, abort_flag,
+                                                              err, kSiteVFull));
+                if (ok && !k_ready)
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKFull + kst), kph, abort_flag,
+                                                              err, kSiteKFull));
+                if (!ok) break;
+                if (leader) {
+                    if (s - 1 >= lo) ptx::mma_commit(bar(C::bVEmpty + vst));
+                    if (s < hi) ptx::mma_commit(bar(C::bKEmpty + kst));
+                }
+                __syncwarp();
             }
             // Every MMA issued above completes before tensor memory is freed.
-            ptx::mma_commit(bar(C::bDrain));
+            if (leader) ptx::mma_commit(bar(C::bDrain));
+            __syncwarp();
             wait_bounded(bar(C::bDrain), 0, nullptr, err, kSiteDrain);
         }
     } else {
         // ------------------------------------------------ softmax, epilogue
         const int t = warp / 4, wq = warp % 4;
+        const Range Rt = (t == 0) ? R[0] : R[1];
         const int r = wq * 32 + lane;
         const int row = q0 + t * BM + r;
         const int row_first = q0 + t * BM;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + C::s_col(t);
         const uint32_t o_addr = tmem + lane_base + C::o_col(t);
-        float m = -INFINITY, l = 0.f;
+        // m_use: the reference the row's P, l and A are currently scaled to.
+        // It moves only when a block's max exceeds it by more than kTau
+        // (log2 units), so P <= 2^kTau and A is rescaled rarely; the final
+        // A / l and lse = m_use + log l are exact for any reference.
+        float m_use = -INFINITY, l = 0.f;
         int c = 0;
         bool ok = true;
-        for (int j = R[t].lo; j < R[t].hi; ++j, ++c) {
+        const float2 c2 = make_float2(scale_log2, scale_log2);
+        for (int j = Rt.lo; j < Rt.hi; ++j, ++c) {
             const bool got = wait_bounded(bar(C::bSFull + t), c & 1, abort_flag, err, kSiteSFull);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -309,40 +386,77 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (!vis) sr[kk] = __float_as_uint(-INFINITY);
                 }
             }
-            float mx = -INFINITY;
+            // row max: four independent chains of three-input max
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int kk = 0; kk < BN; ++kk) mx = fmaxf(mx, __uint_as_float(sr[kk]));
-            const float m_new = fmaxf(m, mx * scale_log2);
-            const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-            float sum = 0.f;
-            uint32_t pk[BN / 2];
-#pragma unroll
-            for (int kk = 0; kk < BN / 2; ++kk) {
-                const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[2 * kk]), scale_log2, -m_ref));
-                const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[2 * kk + 1]), scale_log2, -m_ref));
-                sum += p0 + p1;
-                pk[kk] = pack_bf16x2(p0, p1);
+            for (int kk = 0; kk < BN; kk += 8) {
+                mx0 = ptx::max3(mx0, __uint_as_float(sr[kk]), __uint_as_float(sr[kk + 1]));
+                mx1 = ptx::max3(mx1, __uint_as_float(sr[kk + 2]), __uint_as_float(sr[kk + 3]));
+                mx2 = ptx::max3(mx2, __uint_as_float(sr[kk + 4]), __uint_as_float(sr[kk + 5]));
+                mx3 = ptx::max3(mx3, __uint_as_float(sr[kk + 6]), __uint_as_float(sr[kk + 7]));
             }
-            ptx::tmem_st32x32b_x64(s_addr, pk);
-            const float alpha = ptx::ex2(m - m_ref);
-            l = fmaf(l, alpha, sum);
-            const bool need = (m_new != m) && (m != -INFINITY);
-            if (__any_sync(0xffffffffu, need)) {
+            const float m_blk = ptx::max3(mx0, mx1, fmaxf(mx2, mx3)) * scale_log2;
+            const bool need = m_blk > m_use + kTau;          // false while the block is empty
+            const float m_next = need ? m_blk : m_use;
+            const float m_ref = (m_next == -INFINITY) ? 0.f : m_next;   // the P2 guard
+            const float alpha = need ? ptx::ex2(m_use - m_ref) : 1.f;
+            // P = exp2(S * scale * log2e - m_ref), one 64-key half at a time:
+            // BF16 pairs into tensor memory over S, then signal the MMA warp.
+            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t ov[32];
-                    ptx::tmem_ld32x32b_x32(o_addr + cc * 32, ov);
+            for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                    ptx::tmem_st32x32b_x32(o_addr + cc * 32, ov);
+                for (int q4 = 0; q4 < 2; ++q4) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int kp = 0; kp < 16; kp += 4) {
+                        float2 p[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int kk = half * (BN / 2) + q4 * 32 + 2 * (kp + u);
+                            const float2 x = __ffma2_rn(
+                                make_float2(__uint_as_float(sr[kk]), __uint_as_float(sr[kk + 1])),
+                                c2, nm2);
+                            p[u] = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+                            pk[kp + u] = pack_bf16x2(p[u].x, p[u].y);
+                        }
+                        acc0 = __fadd2_rn(acc0, p[0]);
+                        acc1 = __fadd2_rn(acc1, p[1]);
+                        acc2 = __fadd2_rn(acc2, p[2]);
+                        acc3 = __fadd2_rn(acc3, p[3]);
+                    }
+                    ptx::tmem_st32x32b_x16(s_addr + half * (BN / 4) + q4 * 16, pk);
                 }
+                // Before the first P V product of this block: A <- diag(alpha) A,
+                // only for warps where some row moved its reference (rows that
+                // did not move multiply by exactly 1). Done here, after the
+                // first half of the scores is consumed, to keep registers low.
+                if (half == 0 && __any_sync(0xffffffffu, need && m_use != -INFINITY)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t ov[32];
+                        ptx::tmem_ld32x32b_x32(o_addr + cc * 32, ov);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 r = __fmul2_rn(
+                                make_float2(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])),
+                                make_float2(alpha, alpha));
+                            ov[e] = __float_as_uint(r.x);
+                            ov[e + 1] = __float_as_uint(r.y);
+                        }
+                        ptx::tmem_st32x32b_x32(o_addr + cc * 32, ov);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(C::bPFull + 2 * t + half));
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(C::bPFull + t));
-            m = m_new;
+            const float2 a01 = __fadd2_rn(acc0, acc1), a23 = __fadd2_rn(acc2, acc3);
+            const float2 asum = __fadd2_rn(a01, a23);
+            l = fmaf(l, alpha, asum.x + asum.y);
+            m_use = m_next;
         }
         if (ok && c > 0) {
             const bool got = wait_bounded(bar(C::bODone + t), 0, abort_flag, err, kSiteODone);
@@ -375,7 +489,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         if (lse != nullptr && row < Nq)
             lse[static_cast<long long>(bh) * Nq + row] =
-                (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+                (l > 0.f) ? (m_use + log2f(l)) * kLn2 : -INFINITY;
     }
 
     ptx::tc_fence_before();
