@@ -10,6 +10,8 @@ raises.
 Functions (same names as the C entry points):
   attn_fwd(q, k, v, ...)            BF16 fused forward -> (o, lse)
   attn_fwd_f32(q, k, v, ...)        FP32 fused forward -> (o, lse)
+  attn_fwd_from_host(q, k, v, o, ...)  BF16 forward on host tensors, copies
+                                    pipelined with the kernel by head groups
   attn_decode_workspace_bytes(B, H, d, num_splits)
   attn_decode_splitkv(q, k, v, ...) split-KV decode -> (o, lse)
   attn_decode_splitkv_noalloc(q, k, v, o, ...)  the same, no caller workspace
@@ -244,6 +246,119 @@ def attn_decode_splitkv_noalloc(q, k, v, o, lse=None, scale=None, seqlens_k=None
                                              int(num_splits), _stream_handle(stream, dev))
     _check(st)
     return o, lse
+
+
+class HostPipeline:
+    """Reusable device buffers and streams for ``attn_fwd_from_host``.
+
+    Holds, per in-flight chunk slot, device buffers for q, k, v, o and lse
+    and a compute stream, plus one copy-in and one copy-out stream. Create it
+    once for a shape and reuse it across calls."""
+
+    def __init__(self, B, H, Nq, Nk, d, device=None, chunks=4, dtype=None):
+        import torch
+        dtype = torch.bfloat16 if dtype is None else dtype
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.BH, self.Nq, self.Nk, self.d = B * H, Nq, Nk, d
+        self.B, self.H = B, H
+        self.chunks = max(1, min(int(chunks), self.BH))
+        self.per = -(-self.BH // self.chunks)
+        nslot = min(2, self.chunks)
+        mk = lambda n: torch.empty((self.per, n, d), dtype=dtype, device=self.device)
+        self.slots = [dict(q=mk(Nq), k=mk(Nk), v=mk(Nk), o=mk(Nq),
+                           lse=torch.empty((self.per, Nq), dtype=torch.float32, device=self.device))
+                      for _ in range(nslot)]
+        self.s_in = torch.cuda.Stream(self.device)
+        # one compute stream per slot: a group's kernel can start on SMs that
+        # the previous group's last wave has already left
+        self.s_run = [torch.cuda.Stream(self.device) for _ in self.slots]
+        self.s_out = torch.cuda.Stream(self.device)
+
+
+def attn_fwd_from_host(q, k, v, o, lse=None, scale=None, mask_kind=MASK_NONE, window=0,
+                       seqlens_k=None, pipeline=None, chunks=4):
+    """Fused attention forward for inputs and outputs in (pinned) host memory.
+
+    q [B,H,Nq,d], k/v [B,H,Nk,d] and o [B,H,Nq,d] are CPU tensors (pin them
+    for asynchronous copies; BF16); lse optional CPU FP32 [B,H,Nq]. The
+    (b, h) heads are cut into ``chunks`` contiguous groups: the host-to-device
+    copy of group i+1 and the device-to-host copy of group i-1 overlap the
+    ``attn_fwd`` kernel on group i (two device buffer slots, each with its
+    own compute stream, plus a copy-in and a copy-out stream).
+    Returns after the last copy back has been queued; the caller's current
+    stream is made to wait for it, so synchronising that stream (or the
+    device) makes o / lse readable. seqlens_k (padding mask) is a CPU int32
+    [B] tensor.
+    """
+    import torch
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if pipeline is None:
+        pipeline = HostPipeline(B, H, Nq, Nk, d, device=torch.cuda.current_device(),
+                                chunks=chunks, dtype=q.dtype)
+    P = pipeline
+    if (P.BH, P.Nq, P.Nk, P.d) != (B * H, Nq, Nk, d):
+        raise ValueError("pipeline was built for another shape")
+    qf, kf, vf, of = (t.reshape(B * H, -1, d) for t in (q, k, v, o))
+    lf = lse.reshape(B * H, Nq) if lse is not None else None
+    sl_dev = None
+    if seqlens_k is not None:
+        # one key length per (b, h) so that any group of heads is a batch
+        sl_dev = seqlens_k.to(torch.int32).repeat_interleave(H).to(P.device, non_blocking=True)
+    # the pipeline's streams start after the caller's stream (inputs ready)
+    caller = torch.cuda.current_stream(P.device)
+    P.s_in.wait_stream(caller)
+    for st in P.s_run:
+        st.wait_stream(caller)
+    ev_in = [torch.cuda.Event() for _ in P.slots]
+    ev_run = [torch.cuda.Event() for _ in P.slots]
+    ev_out = [torch.cuda.Event() for _ in P.slots]
+    started = [False] * len(P.slots)
+    for c in range(P.chunks):
+        a, b = c * P.per, min((c + 1) * P.per, B * H)
+        if a >= b:
+            break
+        n = b - a
+        si = c % len(P.slots)
+        S = P.slots[si]
+        with torch.cuda.stream(P.s_in):
+            if started[si]:
+                P.s_in.wait_event(ev_out[si])      # slot's previous results copied out
+            S["q"][:n].copy_(qf[a:b], non_blocking=True)
+            S["k"][:n].copy_(kf[a:b], non_blocking=True)
+            S["v"][:n].copy_(vf[a:b], non_blocking=True)
+            ev_in[si].record(P.s_in)
+        run = P.s_run[si]
+        with torch.cuda.stream(run):
+            run.wait_event(ev_in[si])
+            if sl_dev is None:
+                attn_fwd(S["q"][:n].unsqueeze(0), S["k"][:n].unsqueeze(0),
+                         S["v"][:n].unsqueeze(0), o=S["o"][:n].unsqueeze(0),
+                         lse=S["lse"][:n].unsqueeze(0) if lf is not None else None,
+                         scale=scale, mask_kind=mask_kind, window=window,
+                         stream=run, want_lse=lf is not None)
+            else:
+                _fwd_heads_padded(S, n, sl_dev[a:b], lf is not None, scale, mask_kind, window,
+                                  run)
+            ev_run[si].record(run)
+        with torch.cuda.stream(P.s_out):
+            P.s_out.wait_event(ev_run[si])
+            of[a:b].copy_(S["o"][:n], non_blocking=True)
+            if lf is not None:
+                lf[a:b].copy_(S["lse"][:n], non_blocking=True)
+            ev_out[si].record(P.s_out)
+        started[si] = True
+    caller.wait_stream(P.s_out)
+    return o, lse
+
+
+def _fwd_heads_padded(S, n, sl, want_lse, scale, mask_kind, window, stream):
+    """A group of n heads as a batch of n one-head problems, so that each
+    head carries its own key length."""
+    q, k, v, o = (S[x][:n].unsqueeze(1) for x in ("q", "k", "v", "o"))
+    lse = S["lse"][:n].unsqueeze(1) if want_lse else None
+    return attn_fwd(q, k, v, o=o, lse=lse, scale=scale, mask_kind=mask_kind, window=window,
+                    seqlens_k=sl.contiguous(), stream=stream, want_lse=want_lse)
 
 
 def attn_check_device_error(stream=None):

@@ -287,3 +287,28 @@ def test_bad_arguments_raise(cuda_lib):
     with pytest.raises(cuda_lib.AttnError) as ei:
         cuda_lib.attn_fwd(qm, qm, qm)
     assert ei.value.status == cuda_lib.ATTN_ERR_INVALID_ARG
+
+
+# ------------------------------------------------ host-memory pipelined API
+@pytest.mark.parametrize("shape", [
+    (2, 3, 300, 300, 128, W.MASK_CAUSAL, 0, None, 4),
+    (3, 2, 257, 513, 64, 0, 0, None, 5),
+    (2, 4, 400, 400, 128, W.MASK_WINDOW | W.MASK_PADDING, 96, (0, 400), 3),
+])
+def test_fwd_from_host_matches_device_call(cuda_lib, orc, shape):
+    """attn_fwd_from_host (copies pipelined with the kernel by head groups)
+    gives bit for bit the device-resident attn_fwd result."""
+    B, H, Nq, Nk, d, mk, win, sr, chunks = shape
+    x = W.random_inputs(B, H, Nq, Nk, d, seed=B * 100 + H, seqlen_range=sr)
+    o_dev, l_dev = run_fwd(cuda_lib, x, mk, win)
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.zeros(B, H, Nq, d, dtype=torch.bfloat16).pin_memory()
+    hl = torch.zeros(B, H, Nq, dtype=torch.float32).pin_memory()
+    cuda_lib.attn_fwd_from_host(hq, hk, hv, ho, hl, mask_kind=mk, window=win,
+                                seqlens_k=x["seqlens_k"], chunks=chunks)
+    torch.cuda.synchronize()
+    cuda_lib.attn_check_device_error()
+    assert np.array_equal(ho.float().numpy(), o_dev)
+    assert np.array_equal(hl.numpy(), l_dev)
+    ro, rl = oracle_fwd(orc, x, mk, win)
+    assert_close(ho.float().numpy(), hl.numpy(), ro, rl, TOL_O_BF16, TOL_LSE, what=str(shape))
