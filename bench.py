@@ -211,12 +211,19 @@ def time_loop(fn, steps, warmup, stream, dist_on):
     return total, per
 
 
-def max_over_ranks(x, dist_on):
+def max_over_ranks(x, dist_on, device="cuda"):
+    """The slowest rank's time: every rank gets the max."""
     if not dist_on:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_step, world, steps, total_ms):
+    """Units processed by all ranks per second (replicas: each rank does
+    `units_per_step` per step), timed by the slowest rank."""
+    return units_per_step * world * steps / (total_ms * 1e-3)
 
 
 # -------------------------------------------------------------- our arm
@@ -249,7 +256,7 @@ def run_ours(args, rank, world, dist_on):
     total_ms = max_over_ranks(total_ms, dist_on)
     fl = flops(w)
     ms_step = total_ms / args.steps
-    value = fl * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(fl, world, args.steps, total_ms) / 1e12
     launch_ms = statistics.mean(per)
     achieved = fl / (launch_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2),
