@@ -122,6 +122,47 @@ attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v,
                            attn_stream_t stream);
 
 /*
+ * attn_bwd_workspace_bytes -- bytes of scratch attn_bwd needs: two FP32
+ * values (the row's log-sum-exp in log2 units and D = <dO, O>) per query
+ * row, rows rounded up to a multiple of 128 per (b, h), in two 256-byte
+ * aligned regions. Returns 0 for invalid arguments.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int d);
+
+/*
+ * attn_bwd -- backward pass of attn_fwd, from the saved per-row log-sum-exp.
+ *
+ * The forward keeps only O and lse; the backward rebuilds the normalised
+ * probabilities P = exp(S - lse) block by block with no running max (P1
+ * "What interviewers probe next", on what the backward pass stores; P2
+ * "A strong answer", closing paragraph). With D_i = <dO_i, O_i>:
+ *   dV = P^T dO,  dS = P * (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ * Three launches on `stream`: D and lse into the workspace; a keys-outer
+ * kernel accumulating dK and dV in tensor memory; a queries-outer kernel
+ * accumulating dQ in tensor memory (S and dP are recomputed there).
+ *
+ *   q, k, v      device BF16, as for attn_fwd.
+ *   o            device BF16 [B,H,Nq,d]: the forward output.
+ *   dout         device BF16 [B,H,Nq,d]: gradient of the loss w.r.t. o.
+ *   lse          device FP32 [B,H,Nq]: the forward log-sum-exp (natural
+ *                log; -inf for rows with no visible key).
+ *   dq           device BF16 [B,H,Nq,d] (written).
+ *   dk, dv       device BF16 [B,H,Nk,d] (written; keys no query sees get 0).
+ *   B..window, seqlens_k, stream: exactly the values the forward used.
+ *   workspace    caller-owned device scratch of at least
+ *                attn_bwd_workspace_bytes(B, H, Nq, d) bytes, 256-byte
+ *                aligned; overwritten.
+ * P and dS are rounded to BF16 for the tensor-core products; accumulation
+ * is FP32. Errors: as attn_fwd; ATTN_ERR_INVALID_ARG for a missing or short
+ * workspace.
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       int B, int H, int Nq, int Nk, int d, float scale,
+                       int mask_kind, int window, const int* seqlens_k,
+                       void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * attn_decode_workspace_bytes -- size in bytes of the scratch buffer that
  * attn_decode_splitkv needs for (B, H, d, num_splits): per (b, h, split) one
  * FP32 partial output of d values and one FP32 partial log-sum-exp, at

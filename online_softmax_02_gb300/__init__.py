@@ -12,6 +12,8 @@ Functions (same names as the C entry points):
   attn_fwd_f32(q, k, v, ...)        FP32 fused forward -> (o, lse)
   attn_fwd_from_host(q, k, v, o, ...)  BF16 forward on host tensors, copies
                                     pipelined with the kernel by head groups
+  attn_bwd(q, k, v, o, dout, lse, ...)  backward -> (dq, dk, dv)
+  attn_bwd_workspace_bytes(B, H, Nq, d)
   attn_decode_workspace_bytes(B, H, d, num_splits)
   attn_decode_splitkv(q, k, v, ...) split-KV decode -> (o, lse)
   attn_decode_splitkv_noalloc(q, k, v, o, ...)  the same, no caller workspace
@@ -66,6 +68,10 @@ def load():
     lib.attn_decode_splitkv.restype = I
     lib.attn_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, F, P, I, P]
     lib.attn_decode_splitkv_noalloc.restype = I
+    lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_bwd_workspace_bytes.restype = S
+    lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, P, P, S, P]
+    lib.attn_bwd.restype = I
     lib.attn_check_device_error.argtypes = [P]
     lib.attn_check_device_error.restype = I
     lib.attn_selftest_bounded_wait.argtypes = [ctypes.c_longlong, P]
@@ -163,6 +169,52 @@ def attn_fwd_f32(q, k, v, o=None, lse=None, scale=None, mask_kind=MASK_NONE, win
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     return _fwd(load().attn_fwd_f32, torch.float32, q, k, v, o, lse, scale, mask_kind,
                 window, seqlens_k, stream)
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, Nq: int, d: int) -> int:
+    return int(load().attn_bwd_workspace_bytes(B, H, Nq, d))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, scale=None,
+             mask_kind=MASK_NONE, window=0, seqlens_k=None, workspace=None, stream=None):
+    """Attention backward through ``attn_bwd``: BF16 q, k, v [B,H,N,d], the
+    forward's BF16 output o and FP32 lse [B,H,Nq], and the BF16 gradient
+    dout of the loss with respect to o. Returns (dq, dk, dv) in BF16."""
+    import torch
+    lib = load()
+    _require(q, "q", torch.bfloat16)
+    dev = q.device
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _require(t, n, torch.bfloat16, dev)
+    _require(lse, "lse", torch.float32, dev)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d]")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must have q's shape")
+    if tuple(lse.shape) != (B, H, Nq):
+        raise ValueError("lse must be [B, H, Nq]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _require(t, n, torch.bfloat16, dev)
+    if seqlens_k is not None:
+        _require(seqlens_k, "seqlens_k", torch.int32, dev)
+    need = int(lib.attn_bwd_workspace_bytes(B, H, Nq, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _require(workspace, "workspace", torch.uint8, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(dev):
+        st = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                          _ptr(dk), _ptr(dv), B, H, Nq, Nk, d, float(scale), int(mask_kind),
+                          int(window), _ptr(seqlens_k), _ptr(workspace), workspace.numel(),
+                          _stream_handle(stream, dev))
+    _check(st)
+    return dq, dk, dv
 
 
 def attn_decode_workspace_bytes(B: int, H: int, d: int, num_splits: int) -> int:

@@ -283,6 +283,71 @@ ATTN_API attn_status_t attn_decode_splitkv_noalloc(const void* q, const void* k,
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_splitkv_noalloc kernel launch");
 }
 
+namespace {
+size_t bwd_region(int B, int H, int Nq) {
+    const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(Nq) + 127) / 128 * 128);
+    return align256(rows * sizeof(float));
+}
+}  // namespace
+
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int d) {
+    if (B < 0 || H < 0 || Nq < 0 || (d != 64 && d != 128)) return 0;
+    return 2 * bwd_region(B, H, Nq);
+}
+
+ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int H, int Nq, int Nk, int d, float scale, int mask_kind,
+                                int window, const int* seqlens_k, void* workspace,
+                                size_t workspace_bytes, attn_stream_t stream) {
+    bool nothing = false;
+    attn_status_t st = check_fwd(q, k, v, o, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k,
+                                 &nothing);
+    if (st != ATTN_OK) return st;
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh == 0) return ATTN_OK;
+    if (Nq > 0 && (dout == nullptr || lse == nullptr || dq == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "dout, lse and dq must not be NULL");
+    if (Nk > 0 && (dk == nullptr || dv == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "dk and dv must not be NULL");
+    if ((Nq > 0 && (!aligned16(dout) || !aligned16(dq) ||
+                    (reinterpret_cast<uintptr_t>(lse) & 3u))) ||
+        (Nk > 0 && (!aligned16(dk) || !aligned16(dv))))
+        return fail(ATTN_ERR_INVALID_ARG, "dout, dq, dk, dv must be 16-byte aligned, lse 4-byte");
+    const size_t need = attn_bwd_workspace_bytes(B, H, Nq, d);
+    if (workspace == nullptr || workspace_bytes < need)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
+                    workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (Nq == 0 || Nk == 0) {
+        // no (query, key) pair: every gradient is zero
+        if (Nq > 0 && (e = launch_fill_empty(dq, nullptr, bh * Nq, d, true, s)) != cudaSuccess)
+            return cuda_fail(e, "fill kernel launch");
+        if (Nk > 0) {
+            if ((e = launch_fill_empty(dk, nullptr, bh * Nk, d, true, s)) != cudaSuccess ||
+                (e = launch_fill_empty(dv, nullptr, bh * Nk, d, true, s)) != cudaSuccess)
+                return cuda_fail(e, "fill kernel launch");
+        }
+        return ATTN_OK;
+    }
+    unsigned int* err = nullptr;
+    if ((st = err_word(&err)) != ATTN_OK) return st;
+    CUtensorMap tq, tk, tv, tdo;
+    if ((st = encode_bf16_3d(&tq, q, d, Nq, bh)) != ATTN_OK) return st;
+    if ((st = encode_bf16_3d(&tk, k, d, Nk, bh)) != ATTN_OK) return st;
+    if ((st = encode_bf16_3d(&tv, v, d, Nk, bh)) != ATTN_OK) return st;
+    if ((st = encode_bf16_3d(&tdo, dout, d, Nq, bh)) != ATTN_OK) return st;
+    float* ws_lse2 = static_cast<float*>(workspace);
+    float* ws_dd = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_region(B, H, Nq));
+    BwdArgs a{q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, mask_kind, window,
+              seqlens_k, ws_lse2, ws_dd, err};
+    e = launch_bwd(a, tq, tk, tv, tdo, s);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_bwd kernel launch");
+}
+
 ATTN_API attn_status_t attn_check_device_error(attn_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

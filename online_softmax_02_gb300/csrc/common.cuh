@@ -84,6 +84,20 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // Device address and size of decode.cu's fixed scratch array on the current
 // device (looked up on first use per device).
 cudaError_t decode_static_scratch(void** ptr, size_t* bytes);
+struct BwdArgs {
+    const void* q; const void* k; const void* v; const void* o; const void* dout;
+    const float* lse;
+    void* dq; void* dk; void* dv;
+    int B, H, Nq, Nk, d;
+    float scale;
+    int mask_kind, window;
+    const int* seqlens_k;
+    float* ws_lse2;    // [B*H][Nq rounded up to 128]
+    float* ws_dd;      // same shape
+    unsigned int* err;
+};
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream);
 cudaError_t launch_fill_empty(void* o, float* lse, long long rows, int d, bool bf16,
                               cudaStream_t stream);
 
