@@ -7,8 +7,8 @@ One step = one fused attention forward over the prefill workload
 (B=1, H=64, Nq=Nk=8192, d=128, BF16, no mask), the configuration the
 headline metric is quoted on. The same run also times, each with its own
 warm-up and timed loop, the causal workload (B=2, H=32, 8192^2, causal) and
-the split-KV decode workload (B=1, H=32, Nk=131072, d=128, 64 splits), and
-reports them as sub-objects. Rank 0 prints one JSON line.
+the backward pass on the prefill shape and the split-KV decode workload
+(B=1, H=32, Nk=131072, d=128, 64 splits), and reports them as sub-objects. Rank 0 prints one JSON line.
 
 Inputs are larger than L2 (the prefill inputs are 384 MiB, decode K+V 2 GiB),
 so no L2 flush is done between iterations.
@@ -319,7 +319,7 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
     """The causal and split-KV decode workloads (sub-objects of the line)."""
     import online_softmax_02_gb300 as attn
     if args.only not in ("all", "causal"):
-        return run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result)
+        return run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
     # ---------------- causal workload
     wc = W.CAUSAL
     xc = W.generate(wc)
@@ -343,6 +343,49 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
                                     peaks["bf16_tflops"], 4)}
     del qc, kc, vc, oc, lc, xc
     result["causal"] = causal
+    return run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
+
+
+def run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result):
+    """Backward pass on the prefill shape (B1 H64 8192^2 d128, no mask)."""
+    import online_softmax_02_gb300 as attn
+    if args.only not in ("all", "backward"):
+        return run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result)
+    w = W.PREFILL
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads, name="%s_H%d" % (w.name, args.heads))
+    x = W.generate(w)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    g = torch.Generator("cpu").manual_seed(w.seed + 1)
+    do = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
+    o, lse = attn.attn_fwd(q, k, v, mask_kind=w.mask_kind)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(attn.attn_bwd_workspace_bytes(w.B, w.H, w.Nq, w.d), dtype=torch.uint8,
+                     device=dev)
+
+    def step_b():
+        attn.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, mask_kind=w.mask_kind,
+                      workspace=ws, stream=stream)
+
+    b_steps = max(3, args.steps // 4)
+    b_total, b_per = time_loop(step_b, b_steps, args.warmup, stream, dist_on)
+    attn.attn_check_device_error(stream)
+    b_total = max_over_ranks(b_total, dist_on)
+    fl = 2.5 * flops(w)          # five products of 2 d FLOPs per visible pair
+    b_ms = statistics.mean(b_per)
+    achieved = fl / (b_ms * 1e-3) / 1e12
+    result["backward"] = {
+        "metric": "attn bwd TFLOP/s", "config": w.describe(),
+        "ms_per_step": round(b_total / b_steps, 4),
+        "value": round(whole_job_rate(fl, world, b_steps, b_total) / 1e12, 2), "unit": "TFLOP/s",
+        "flop_count": "2.5x forward (5 products: S, dP, dV, dK, dQ); the kernels execute 7 "
+                      "(S and dP are recomputed for dQ)",
+        "gpu_launches_per_step": 3,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": None, "note": "time of the three launches per step"}}
+    del q, k, v, do, o, lse, dq, dk, dv, ws, x
     return run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result)
 
 
@@ -456,7 +499,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8, help="head groups of the e2e pipeline")
     # profiling helpers: run one section, or a reduced size of it
-    ap.add_argument("--only", choices=["all", "prefill", "causal", "decode"], default="all")
+    ap.add_argument("--only", choices=["all", "prefill", "causal", "backward", "decode"],
+                    default="all")
     ap.add_argument("--heads", type=int, default=0, help="override H of the prefill workload")
     ap.add_argument("--decode-nk", type=int, default=0, help="override Nk of the decode workload")
     args = ap.parse_args()
