@@ -7,8 +7,10 @@ never imports this package.
 
 Contents
   * ``attn_oracle.c`` (loaded here through ctypes): the plain three-pass
-    definition of masked softmax attention plus the per-row log-sum-exp, in
-    double precision. See the header of that file for the steps and citations.
+    definition of masked softmax attention plus the per-row log-sum-exp, and
+    the plain three-pass row softmax, in double precision. See the header of
+    that file for the steps and citations.
+  * ``backward.py``: the chain-rule gradients of attention in FP64.
   * ``recurrence.py``: the online (m, l) pair update, its merge, and the
     blockwise query-tile recurrence, written from the pages' equations. They
     are used only to cross-check the direct definition above.
@@ -73,6 +75,10 @@ class Oracle:
             ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_int]
         self._lib.oracle_max_threads.restype = ctypes.c_int
+        g = self._lib.oracle_softmax_rows
+        g.restype = ctypes.c_int
+        g.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_void_p,
+                      ctypes.c_void_p, ctypes.c_int]
 
     def attention(self, q, k, v, scale, mask_kind=MASK_NONE, window=0,
                   seqlens_k=None, rows=None, threads=None):
@@ -120,6 +126,21 @@ class Oracle:
         if rows is None:
             return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
         return o, lse
+
+    def softmax_rows(self, x, threads=None):
+        """Row softmax of x [rows, n] in FP64 (three-pass safe softmax).
+        Returns (y [rows, n], lse [rows]) as float64."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        if x.ndim != 2:
+            raise ValueError("x must be [rows, n]")
+        rows, n = x.shape
+        y = np.zeros((rows, n), dtype=np.float64)
+        lse = np.zeros(rows, dtype=np.float64)
+        rc = self._lib.oracle_softmax_rows(x.ctypes.data, rows, n, y.ctypes.data,
+                                           lse.ctypes.data, threads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle_softmax_rows failed with code %d" % rc)
+        return y, lse
 
     def max_threads(self) -> int:
         return int(self._lib.oracle_max_threads())

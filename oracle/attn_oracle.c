@@ -171,3 +171,30 @@ int oracle_max_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * oracle_softmax_rows: row softmax of x [rows, n] (FP32 values upcast to
+ * double), the three-pass "safe softmax" of P3 "Step 1": the row maximum,
+ * the sum of exp(x - m), then each output exp(x_i - m) / sum. Also writes the
+ * row's log-sum-exp m + log(sum). Outputs in double.
+ */
+int oracle_softmax_rows(const float* x, long long rows, long long n, double* y, double* lse,
+                        int nthreads)
+{
+    if (rows < 0 || n <= 0) return -1;
+    if (nthreads <= 0) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nthreads)
+    for (long long r = 0; r < rows; ++r) {
+        const float* xr = x + r * n;
+        double* yr = y + r * n;
+        double mx = -INFINITY;                      /* pass 1: maximum   */
+        for (long long i = 0; i < n; ++i)
+            if ((double)xr[i] > mx) mx = (double)xr[i];
+        double sum = 0.0;                           /* pass 2: normalizer */
+        for (long long i = 0; i < n; ++i) sum += exp((double)xr[i] - mx);
+        for (long long i = 0; i < n; ++i)           /* pass 3: outputs    */
+            yr[i] = exp((double)xr[i] - mx) / sum;
+        lse[r] = mx + log(sum);
+    }
+    return 0;
+}
