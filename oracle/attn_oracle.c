@@ -176,7 +176,9 @@ int oracle_max_threads(void)
  * oracle_softmax_rows: row softmax of x [rows, n] (FP32 values upcast to
  * double), the three-pass "safe softmax" of P3 "Step 1": the row maximum,
  * the sum of exp(x - m), then each output exp(x_i - m) / sum. Also writes the
- * row's log-sum-exp m + log(sum). Outputs in double.
+ * row's log-sum-exp m + log(sum). Outputs in double. A row whose entries
+ * are all -inf (fully masked) gives y = 0 and lse = -inf, the same reading as
+ * an attention row with no visible key.
  */
 int oracle_softmax_rows(const float* x, long long rows, long long n, double* y, double* lse,
                         int nthreads)
@@ -190,6 +192,11 @@ int oracle_softmax_rows(const float* x, long long rows, long long n, double* y, 
         double mx = -INFINITY;                      /* pass 1: maximum   */
         for (long long i = 0; i < n; ++i)
             if ((double)xr[i] > mx) mx = (double)xr[i];
+        if (mx == -INFINITY) {          /* every entry -inf: y = 0, lse = -inf */
+            for (long long i = 0; i < n; ++i) yr[i] = 0.0;
+            lse[r] = -INFINITY;
+            continue;
+        }
         double sum = 0.0;                           /* pass 2: normalizer */
         for (long long i = 0; i < n; ++i) sum += exp((double)xr[i] - mx);
         for (long long i = 0; i < n; ++i)           /* pass 3: outputs    */

@@ -64,7 +64,22 @@ def pin_sm_large_scores(orc):
         assert not np.all(np.isfinite(naive))
 
 
-SM_PINS = [pin_sm_worked_example, pin_sm_library, pin_sm_online_pairs, pin_sm_large_scores]
+def pin_sm_masked_entries(orc):
+    """-inf entries get weight 0 (torch agrees); an all -inf row gives 0 and
+    lse = -inf, no NaN."""
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((3, 40)).astype(np.float32)
+    x[0, ::3] = -np.inf
+    x[2, :] = -np.inf
+    y, lse = orc.softmax_rows(x)
+    t = torch.from_numpy(x[:2]).double()
+    assert np.abs(torch.softmax(t, dim=1).numpy() - y[:2]).max() <= 8e-15
+    assert np.all(y[0, ::3] == 0)
+    assert np.all(y[2] == 0) and lse[2] == -np.inf and not np.isnan(y).any()
+
+
+SM_PINS = [pin_sm_worked_example, pin_sm_library, pin_sm_online_pairs, pin_sm_large_scores,
+           pin_sm_masked_entries]
 
 
 @pytest.mark.parametrize("pin", SM_PINS, ids=lambda f: f.__name__)
