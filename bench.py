@@ -392,7 +392,7 @@ def run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
 def run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result):
     import online_softmax_02_gb300 as attn
     if args.only not in ("all", "decode"):
-        return result
+        return run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result)
     # ---------------- split-KV decode
     wd = W.DECODE
     if args.decode_nk:
@@ -427,7 +427,92 @@ def run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result):
                            "note": "time is both launches (split + combine) per step"}}
     del qd, kd, vd, xd
     result["decode"] = decode
+    return run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result)
+
+
+def run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result):
+    """Standalone row softmax, [4096, 32768] FP32."""
+    import online_softmax_02_gb300 as attn
+    if args.only not in ("all", "softmax"):
+        return result
+    x = W.softmax_inputs().to(dev)
+    y = torch.empty_like(x)
+    lse = torch.empty(x.shape[0], dtype=torch.float32, device=dev)
+
+    def step_s():
+        attn.attn_softmax_rows(x, y=y, lse=lse, stream=stream)
+
+    s_total, s_per = time_loop(step_s, args.steps, args.warmup, stream, dist_on)
+    attn.attn_check_device_error(stream)
+    s_total = max_over_ranks(s_total, dist_on)
+    alg = 2 * x.numel() * x.element_size() + lse.numel() * 4     # read x once, write y and lse
+    gbs = alg / (statistics.mean(s_per) * 1e-3) / 1e9
+    result["softmax"] = {
+        "metric": "row softmax HBM GB/s", "config": {"workload": "softmax_rows_4096x32768_f32",
+                                                     "rows": x.shape[0], "n": x.shape[1]},
+        "ms_per_step": round(s_total / args.steps, 4),
+        "value": round(whole_job_rate(alg, world, args.steps, s_total) / 1e9, 1), "unit": "GB/s",
+        "gpu_launches_per_step": 1,
+        "bytes_note": "algorithmic bytes = one HBM read of x, one write of y, the lse; the "
+                      "two-pass method's second read of each row is served by L2 (rows of "
+                      "128 KiB, 512 threads per row)",
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None}}
+    del x, y, lse
+    if not args.no_naive:
+        result["softmax"]["naive_attention_context"] = naive_attention_context(args, dev, stream,
+                                                                               peaks)
     return result
+
+
+def naive_attention_context(args, dev, stream, peaks):
+    """Context only (not a product path): attention with the score matrix in
+    HBM, as costed in P1 "Now the cost" -- S = scale*Q K^T written by a library
+    GEMM, read by the row softmax which writes P, P read by a second library
+    GEMM -- beside the fused forward on the same inputs (prefill shape)."""
+    import online_softmax_02_gb300 as attn
+    w = W.PREFILL
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads)
+    x = W.generate(w)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    qs = (q.float() * w.scale).to(torch.bfloat16)      # scale folded into Q (context only)
+    B, H, N, d = q.shape
+    S = torch.empty(B, H, N, N, dtype=torch.bfloat16, device=dev)
+    P = torch.empty_like(S)
+    o = torch.empty_like(q)
+    lse = torch.empty(B * H * N, dtype=torch.float32, device=dev)
+    fl = flops(w)
+
+    def naive():
+        with torch.cuda.stream(stream):
+            torch.matmul(qs, k.transpose(-1, -2), out=S)
+            attn.attn_softmax_rows(S.view(-1, N), y=P.view(-1, N), lse=lse, stream=stream)
+            torch.matmul(P, v, out=o)
+
+    def softmax_only():
+        attn.attn_softmax_rows(S.view(-1, N), y=P.view(-1, N), lse=lse, stream=stream)
+
+    def fused():
+        attn.attn_fwd(q, k, v, o=o, mask_kind=w.mask_kind, stream=stream)
+
+    steps, warm = 10, 3
+    t_naive = time_loop(naive, steps, warm, stream, False)[0] / steps
+    t_sm = time_loop(softmax_only, steps, warm, stream, False)[0] / steps
+    t_fused = time_loop(fused, steps, warm, stream, False)[0] / steps
+    attn.attn_check_device_error(stream)
+    score_bytes = 4 * S.numel() * S.element_size()     # S written + read, P written + read
+    out = {"workload": w.name, "score_matrix_bytes_each": S.numel() * S.element_size(),
+           "score_traffic_bytes": score_bytes,
+           "score_traffic_floor_ms": round(score_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3, 3),
+           "naive_ms": round(t_naive, 3), "naive_softmax_ms": round(t_sm, 3),
+           "fused_ms": round(t_fused, 3), "naive_over_fused": round(t_naive / t_fused, 2),
+           "naive_tflops": round(fl / (t_naive * 1e-3) / 1e12, 1),
+           "fused_tflops": round(fl / (t_fused * 1e-3) / 1e12, 1),
+           "gemms": "torch.matmul (cuBLAS), BF16 S and P; the softmax is attn_softmax_rows"}
+    del S, P
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------ oracle on the host
@@ -499,8 +584,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8, help="head groups of the e2e pipeline")
     # profiling helpers: run one section, or a reduced size of it
-    ap.add_argument("--only", choices=["all", "prefill", "causal", "backward", "decode"],
-                    default="all")
+    ap.add_argument("--no-naive", action="store_true",
+                    help="skip the naive (score matrix in HBM) attention context measurement")
+    ap.add_argument("--only", choices=["all", "prefill", "causal", "backward", "decode",
+                                       "softmax"], default="all")
     ap.add_argument("--heads", type=int, default=0, help="override H of the prefill workload")
     ap.add_argument("--decode-nk", type=int, default=0, help="override Nk of the decode workload")
     args = ap.parse_args()

@@ -76,6 +76,12 @@ enum {
     ATTN_MASK_PADDING = 4
 };
 
+/* Element types of attn_softmax_rows. */
+enum {
+    ATTN_DTYPE_F32 = 0,
+    ATTN_DTYPE_BF16 = 1
+};
+
 /* Opaque CUDA stream handle (cudaStream_t / CUstream). */
 typedef void* attn_stream_t;
 
@@ -233,6 +239,26 @@ attn_status_t attn_decode_splitkv_noalloc(const void* q, const void* k, const vo
                                           int B, int H, int Nk, int d, float scale,
                                           const int* seqlens_k, int num_splits,
                                           attn_stream_t stream);
+
+/*
+ * attn_softmax_rows -- row softmax y = softmax(x) of a [rows, n] matrix with
+ * the online normalizer (P3 "Online softmax": "Step 2" keeps the pair
+ * (m, l) -- running maximum and sum of exp(x - m), the sum rescaled by
+ * exp(m_old - m_new) when the maximum grows -- in one pass; "Step 3" writes
+ * exp(x_i - m) / l in a second pass; "Step 4" merges the pairs of the
+ * threads that share a row, in any grouping).
+ *
+ *   x, y     device pointers, [rows, n] row-major, same dtype (ATTN_DTYPE_F32
+ *            or ATTN_DTYPE_BF16), aligned to the element size (16-byte
+ *            aligned rows with n a multiple of 16 bytes take the vector path).
+ *            x and y may be the same buffer.
+ *   lse      device FP32 [rows] (written: m + log l, natural log), or NULL.
+ *   rows     0 <= rows < 2^31; n >= 1.
+ * Entries may be -inf (weight 0); a row of only -inf gives y = 0 and
+ * lse = -inf. Arithmetic is FP32; BF16 outputs are rounded once.
+ */
+attn_status_t attn_softmax_rows(const void* x, void* y, float* lse, long long rows, int n,
+                                int dtype, attn_stream_t stream);
 
 /*
  * attn_check_device_error -- synchronise `stream`, then report whether any

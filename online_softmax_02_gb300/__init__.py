@@ -17,6 +17,7 @@ Functions (same names as the C entry points):
   attn_decode_workspace_bytes(B, H, d, num_splits)
   attn_decode_splitkv(q, k, v, ...) split-KV decode -> (o, lse)
   attn_decode_splitkv_noalloc(q, k, v, o, ...)  the same, no caller workspace
+  attn_softmax_rows(x, ...)         standalone row softmax -> (y, lse)
   attn_check_device_error(stream=None)
   attn_selftest_bounded_wait(limit_cycles, stream=None)
 """
@@ -72,6 +73,8 @@ def load():
     lib.attn_bwd_workspace_bytes.restype = S
     lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, P, P, S, P]
     lib.attn_bwd.restype = I
+    lib.attn_softmax_rows.argtypes = [P, P, P, ctypes.c_longlong, I, I, P]
+    lib.attn_softmax_rows.restype = I
     lib.attn_check_device_error.argtypes = [P]
     lib.attn_check_device_error.restype = I
     lib.attn_selftest_bounded_wait.argtypes = [ctypes.c_longlong, P]
@@ -411,6 +414,29 @@ def _fwd_heads_padded(S, n, sl, want_lse, scale, mask_kind, window, stream):
     lse = S["lse"][:n].unsqueeze(1) if want_lse else None
     return attn_fwd(q, k, v, o=o, lse=lse, scale=scale, mask_kind=mask_kind, window=window,
                     seqlens_k=sl.contiguous(), stream=stream, want_lse=want_lse)
+
+
+def attn_softmax_rows(x, y=None, lse=None, stream=None, want_lse=True):
+    """Row softmax of a 2-D CUDA tensor (FP32 or BF16) through
+    ``attn_softmax_rows``; returns (y, lse)."""
+    import torch
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be float32 or bfloat16")
+    _require(x, "x", x.dtype)
+    if x.dim() != 2:
+        raise ValueError("x must be [rows, n]")
+    y = torch.empty_like(x) if y is None else y
+    _require(y, "y", x.dtype, x.device)
+    if lse is None and want_lse:
+        lse = torch.empty(x.shape[0], dtype=torch.float32, device=x.device)
+    if lse is not None:
+        _require(lse, "lse", torch.float32, x.device)
+    dtype = 1 if x.dtype == torch.bfloat16 else 0
+    with torch.cuda.device(x.device):
+        st = load().attn_softmax_rows(_ptr(x), _ptr(y), _ptr(lse), x.shape[0], x.shape[1], dtype,
+                                      _stream_handle(stream, x.device))
+    _check(st)
+    return y, lse
 
 
 def attn_check_device_error(stream=None):

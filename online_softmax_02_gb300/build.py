@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build", "attn")
 LIB = os.path.join(PKG, "libattn.so")
-SOURCES = ["attn_api.cu", "fwd_sm103.cu", "bwd_sm103.cu", "fwd_f32.cu", "decode.cu"]
+SOURCES = ["attn_api.cu", "fwd_sm103.cu", "bwd_sm103.cu", "fwd_f32.cu", "decode.cu", "softmax.cu"]
 HEADERS = ["common.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",

@@ -348,6 +348,25 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_bwd kernel launch");
 }
 
+ATTN_API attn_status_t attn_softmax_rows(const void* x, void* y, float* lse, long long rows,
+                                         int n, int dtype, attn_stream_t stream) {
+    if (rows < 0 || rows > 2147483647LL || n < 1)
+        return fail(ATTN_ERR_INVALID_ARG, "rows must be in [0, 2^31), n >= 1 (rows=%lld n=%d)",
+                    rows, n);
+    if (dtype != ATTN_DTYPE_F32 && dtype != ATTN_DTYPE_BF16)
+        return fail(ATTN_ERR_UNSUPPORTED, "dtype %d (ATTN_DTYPE_F32 or ATTN_DTYPE_BF16)", dtype);
+    if (rows == 0) return ATTN_OK;
+    if (x == nullptr || y == nullptr) return fail(ATTN_ERR_INVALID_ARG, "x and y must not be NULL");
+    const size_t esz = dtype == ATTN_DTYPE_BF16 ? 2 : 4;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & (esz - 1))
+        return fail(ATTN_ERR_INVALID_ARG, "x and y must be aligned to their element size");
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    cudaError_t e = launch_softmax_rows(x, y, lse, rows, n, dtype == ATTN_DTYPE_BF16,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_softmax_rows kernel launch");
+}
+
 ATTN_API attn_status_t attn_check_device_error(attn_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

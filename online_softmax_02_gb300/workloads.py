@@ -22,6 +22,8 @@ figures they discuss):
                [100, 4096], sliding window 1024 plus padding.
   decode       B=1, H=32, one query per head, Nk=131072, d=128, BF16,
                64 key splits.
+  softmax      [4096, 32768] FP32 scores, N(0, 1): batches of long vectors
+               as in the row-softmax measurements the pages quote.
 """
 from __future__ import annotations
 
@@ -123,6 +125,16 @@ def generate(w: Workload):
         v = torch.randn(w.B, w.H, w.Nk, w.d, generator=g, dtype=torch.float32)
     q, k, v = (t.to(w.dtype).contiguous() for t in (q, k, v))
     return {"q": q, "k": k, "v": v, "seqlens_k": seqlens}
+
+
+SOFTMAX_ROWS, SOFTMAX_N = 4096, 32768    # row softmax workload: [4096, 32768] FP32
+
+
+def softmax_inputs(rows=SOFTMAX_ROWS, n=SOFTMAX_N, dtype=torch.float32, seed=0, scale=1.0):
+    """Seeded [rows, n] matrix of N(0, scale^2) scores (drawn in FP32, rounded
+    once to `dtype`), the input of the standalone row softmax."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    return (torch.randn(rows, n, generator=g, dtype=torch.float32) * scale).to(dtype).contiguous()
 
 
 def random_inputs(B, H, Nq, Nk, d, dtype=torch.bfloat16, seed=0,
