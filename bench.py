@@ -51,8 +51,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum), keyed by the source file of the kernel and its
 # SHA-256 at capture time; reported as null when the source has changed.
 NCU_TRAFFIC = {
-    "fwd_sm103.cu": None,   # {"sha256": ..., "bytes_per_launch": ..., "workload": ...}
-    "decode.cu": None,
+    # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
+    # launch at the full bench workload, 1-pass ncu capture (profiles/
+    # ncu_traffic_full_size.md); valid while the kernel source is unchanged.
+    "fwd_sm103.cu": {"sha256": "99b536f424a8e2839c22254126fc4572b6b233be423d49920443f8516f56a1e8",
+                     "bytes_per_launch": 403241984 + 114888704,
+                     "workload": "prefill_B1_H64_N8192_d128_bf16"},
+    "decode.cu": {"sha256": "1307a0be67d90977d4847a9f6c760c5b2d48dad081c5b803233a750d89e4f405",
+                  "bytes_per_launch": 2147748864 + 3136768,
+                  "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split kernel)"},
+    "softmax.cu": {"sha256": "9a40d74a21d385c58919240ac5c54e555e31ccc3e2bd568868bc0f51f562068d",
+                   "bytes_per_launch": 537604096 + 475967488,
+                   "workload": "softmax_rows_4096x32768_f32"},
 }
 
 
@@ -262,7 +272,7 @@ def run_ours(args, rank, world, dist_on):
     roofline = {"bound": "tensor", "achieved": round(achieved, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": traffic_for("fwd_sm103.cu"),
+                "traffic": traffic_for("fwd_sm103.cu", w.H / W.PREFILL.H),
                 "peak_source": "%s bf16_tflops (burst) from MEASURED_PEAKS.json" % peak_src
                 if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
                 "kernel": "fwd_sm103_kernel<128>",
@@ -422,7 +432,7 @@ def run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result):
               "workspace_bytes_per_step": int(2 * ws.numel()),
               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                           "traffic": traffic_for("decode.cu"),
+                           "traffic": traffic_for("decode.cu", wd.Nk / W.DECODE.Nk),
                            "algorithmic_bytes_per_step": alg_bytes,
                            "note": "time is both launches (split + combine) per step"}}
     del qd, kd, vd, xd
@@ -435,7 +445,7 @@ def run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result):
     import online_softmax_02_gb300 as attn
     if args.only not in ("all", "softmax"):
         return result
-    x = W.softmax_inputs().to(dev)
+    x = W.softmax_inputs(rows=args.softmax_rows or W.SOFTMAX_ROWS).to(dev)
     y = torch.empty_like(x)
     lse = torch.empty(x.shape[0], dtype=torch.float32, device=dev)
 
@@ -448,8 +458,9 @@ def run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result):
     alg = 2 * x.numel() * x.element_size() + lse.numel() * 4     # read x once, write y and lse
     gbs = alg / (statistics.mean(s_per) * 1e-3) / 1e9
     result["softmax"] = {
-        "metric": "row softmax HBM GB/s", "config": {"workload": "softmax_rows_4096x32768_f32",
-                                                     "rows": x.shape[0], "n": x.shape[1]},
+        "metric": "row softmax HBM GB/s",
+        "config": {"workload": "softmax_rows_%dx%d_f32" % tuple(x.shape),
+                   "rows": x.shape[0], "n": x.shape[1]},
         "ms_per_step": round(s_total / args.steps, 4),
         "value": round(whole_job_rate(alg, world, args.steps, s_total) / 1e9, 1), "unit": "GB/s",
         "gpu_launches_per_step": 1,
@@ -457,7 +468,8 @@ def run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result):
                       "two-pass method's second read of each row is served by L2 (rows of "
                       "128 KiB, 512 threads per row)",
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None}}
+                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "traffic": traffic_for("softmax.cu", x.shape[0] / W.SOFTMAX_ROWS)}}
     del x, y, lse
     if not args.no_naive:
         result["softmax"]["naive_attention_context"] = naive_attention_context(args, dev, stream,
@@ -590,6 +602,8 @@ def main():
                                        "softmax"], default="all")
     ap.add_argument("--heads", type=int, default=0, help="override H of the prefill workload")
     ap.add_argument("--decode-nk", type=int, default=0, help="override Nk of the decode workload")
+    ap.add_argument("--softmax-rows", type=int, default=0,
+                    help="override the row count of the softmax workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
