@@ -329,7 +329,7 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
     """The causal and split-KV decode workloads (sub-objects of the line)."""
     import online_softmax_02_gb300 as attn
     if args.only not in ("all", "causal"):
-        return run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
+        return run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result)
     # ---------------- causal workload
     wc = W.CAUSAL
     xc = W.generate(wc)
@@ -353,6 +353,42 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
                                     peaks["bf16_tflops"], 4)}
     del qc, kc, vc, oc, lc, xc
     result["causal"] = causal
+    return run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result)
+
+
+def run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result):
+    """The prefill workload with Q, K, V stored as E4M3 (attn_fwd_fp8)."""
+    import online_softmax_02_gb300 as attn
+    if args.only not in ("all", "fp8"):
+        return run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
+    w = W.PREFILL
+    if args.heads:
+        w = dataclasses.replace(w, H=args.heads, name="%s_H%d" % (w.name, args.heads))
+    x = W.generate_fp8(w)
+    w = dataclasses.replace(w, name=w.name.replace("bf16", "e4m3"))
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+
+    def step_f():
+        attn.attn_fwd_fp8(q, k, v, x["descale_q"], x["descale_k"], x["descale_v"], o=o, lse=lse,
+                          stream=stream)
+
+    f_total, f_per = time_loop(step_f, args.steps, args.warmup, stream, dist_on)
+    attn.attn_check_device_error(stream)
+    f_total = max_over_ranks(f_total, dist_on)
+    fl = flops(w)
+    achieved = fl / (statistics.mean(f_per) * 1e-3) / 1e12
+    peak8 = 2.0 * peaks["bf16_tflops"]
+    result["fp8"] = {
+        "config": dict(w.describe(), dtype="e4m3", descale="per tensor, power of two"),
+        "ms_per_step": round(f_total / args.steps, 4),
+        "value": round(whole_job_rate(fl, world, args.steps, f_total) / 1e12, 2),
+        "unit": "TFLOP/s", "gpu_launches_per_step": 1,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak8, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / peak8, 4), "traffic": None,
+                     "peak_note": "measured bf16 burst x 2 (nominal e4m3 / bf16 dense ratio)"}}
+    del q, k, v, o, lse, x
     return run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
 
 
@@ -598,7 +634,7 @@ def main():
     # profiling helpers: run one section, or a reduced size of it
     ap.add_argument("--no-naive", action="store_true",
                     help="skip the naive (score matrix in HBM) attention context measurement")
-    ap.add_argument("--only", choices=["all", "prefill", "causal", "backward", "decode",
+    ap.add_argument("--only", choices=["all", "prefill", "causal", "fp8", "backward", "decode",
                                        "softmax"], default="all")
     ap.add_argument("--heads", type=int, default=0, help="override H of the prefill workload")
     ap.add_argument("--decode-nk", type=int, default=0, help="override Nk of the decode workload")

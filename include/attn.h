@@ -117,6 +117,34 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v,
                        attn_stream_t stream);
 
 /*
+ * attn_fwd_fp8 -- attn_fwd with 8-bit floating-point inputs, the FP8 mode P1
+ * ("What did FlashAttention-2 and -3 change?") and P3 ("Where the merge is
+ * used today") credit to FlashAttention-3. q, k and v hold E4M3 values
+ * (1 sign, 4 exponent, 3 mantissa bits, bias 7, no infinities; one byte
+ * each, layout as attn_fwd); the real inputs are q*descale_q, k*descale_k
+ * and v*descale_v, per-tensor factors chosen by the caller when quantising.
+ * Computed: O = softmax(scale * Q K^T + mask) V and lse on those real
+ * values, with both products on the 8-bit tensor-core path (FP32
+ * accumulation) and the attention weights rounded to E4M3 for the P V
+ * product; the row sums l, the running maxima and the accumulator are FP32.
+ *
+ *   q, k, v      device E4M3 pointers, [B,H,N,128], 16-byte aligned.
+ *   o            device BF16 [B,H,Nq,128] (written).
+ *   lse          device FP32 [B,H,Nq] (written), natural log of the real
+ *                scores' sum of exponentials; may be NULL.
+ *   d            must be 128 (ATTN_ERR_UNSUPPORTED otherwise).
+ *   descale_*    finite and > 0; scale * descale_q * descale_k * log2(e)
+ *                must be finite in FP32.
+ *   others       as attn_fwd (masks, empty rows, errors, stream).
+ */
+attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v,
+                           void* o, float* lse,
+                           int B, int H, int Nq, int Nk, int d, float scale,
+                           float descale_q, float descale_k, float descale_v,
+                           int mask_kind, int window, const int* seqlens_k,
+                           attn_stream_t stream);
+
+/*
  * attn_fwd_f32 -- the same operation with FP32 q, k, v and o (lse FP32).
  * All arithmetic is FP32 on the CUDA cores; intended for accuracy checks of
  * small problems such as P2's 1,000-key tile test. Arguments as attn_fwd.

@@ -63,6 +63,8 @@ def load():
     lib.attn_fwd.restype = I
     lib.attn_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, P]
     lib.attn_fwd_f32.restype = I
+    lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, F, F, I, I, P, P]
+    lib.attn_fwd_fp8.restype = I
     lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I]
     lib.attn_decode_workspace_bytes.restype = S
     lib.attn_decode_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, F, P, I, P, S, P]
@@ -115,8 +117,10 @@ def _require(t, name, dtype, device=None):
         raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
 
 
-def _fwd(fn, dtype, q, k, v, o, lse, scale, mask_kind, window, seqlens_k, stream):
+def _fwd(fn, dtype, q, k, v, o, lse, scale, mask_kind, window, seqlens_k, stream,
+         out_dtype=None, descales=()):
     import torch
+    out_dtype = dtype if out_dtype is None else out_dtype
     _require(q, "q", dtype)
     dev = q.device
     _require(k, "k", dtype, dev)
@@ -128,8 +132,8 @@ def _fwd(fn, dtype, q, k, v, o, lse, scale, mask_kind, window, seqlens_k, stream
     if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
         raise ValueError("k and v must be [B, H, Nk, d] matching q")
     if o is None:
-        o = torch.empty_like(q)
-    _require(o, "o", dtype, dev)
+        o = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    _require(o, "o", out_dtype, dev)
     if tuple(o.shape) != tuple(q.shape):
         raise ValueError("o must have q's shape")
     if lse is not None:
@@ -144,8 +148,8 @@ def _fwd(fn, dtype, q, k, v, o, lse, scale, mask_kind, window, seqlens_k, stream
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(dev):
         st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
-                float(scale), int(mask_kind), int(window), _ptr(seqlens_k),
-                _stream_handle(stream, dev))
+                float(scale), *[float(f) for f in descales], int(mask_kind), int(window),
+                _ptr(seqlens_k), _stream_handle(stream, dev))
     _check(st)
     return o, lse
 
@@ -162,6 +166,21 @@ def attn_fwd(q, k, v, o=None, lse=None, scale=None, mask_kind=MASK_NONE, window=
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     return _fwd(load().attn_fwd, torch.bfloat16, q, k, v, o, lse, scale, mask_kind,
                 window, seqlens_k, stream)
+
+
+def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, o=None, lse=None, scale=None,
+                 mask_kind=MASK_NONE, window=0, seqlens_k=None, stream=None, want_lse=True):
+    """E4M3 fused attention forward through ``attn_fwd_fp8``.
+
+    q [B,H,Nq,128], k/v [B,H,Nk,128] contiguous ``torch.float8_e4m3fn`` CUDA
+    tensors holding the inputs divided by their per-tensor factors
+    ``descale_*``; returns (o [B,H,Nq,128] BF16, lse [B,H,Nq] FP32 or None)."""
+    import torch
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    return _fwd(load().attn_fwd_fp8, torch.float8_e4m3fn, q, k, v, o, lse, scale, mask_kind,
+                window, seqlens_k, stream, out_dtype=torch.bfloat16,
+                descales=(descale_q, descale_k, descale_v))
 
 
 def attn_fwd_f32(q, k, v, o=None, lse=None, scale=None, mask_kind=MASK_NONE, window=0,

@@ -20,6 +20,9 @@ namespace attn {
 
 cudaError_t launch_fwd_sm103_maps(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                   const CUtensorMap& tv, cudaStream_t stream);
+cudaError_t launch_fwd_fp8_maps(const FwdArgs& a, float descale_q, float descale_k,
+                                float descale_v, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, cudaStream_t stream);
 
 namespace {
 
@@ -76,22 +79,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D BF16 tensor map over [B*H][rows][d] with a 64 x 128 x 1 box and
-// 128-byte swizzle (one swizzle atom row = 64 BF16 head dims).
-attn_status_t encode_bf16_3d(CUtensorMap* m, const void* ptr, int d, int rows, long long bh) {
+// 3-D tensor map over [B*H][rows][d] with 128-byte swizzle and a box of one
+// swizzle atom row (128 bytes: 64 BF16 or 128 8-bit head dims) x 128 rows x 1.
+attn_status_t encode_3d(CUtensorMap* m, const void* ptr, int d, int rows, long long bh,
+                        bool one_byte) {
     auto fn = encode_fn();
     if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+    const cuuint64_t esz = one_byte ? 1 : 2;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                           static_cast<cuuint64_t>(bh)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                             static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz,
+                             static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d) * esz};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = fn(m, one_byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    3, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return ATTN_OK;
+}
+
+attn_status_t encode_bf16_3d(CUtensorMap* m, const void* ptr, int d, int rows, long long bh) {
+    return encode_3d(m, ptr, d, rows, bh, false);
 }
 
 __global__ void fill_empty_kernel(void* o, float* lse, long long rows, int d, int is_bf16) {
@@ -175,6 +185,42 @@ ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, voi
     FwdArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k, err};
     cudaError_t e = launch_fwd_sm103_maps(a, tq, tk, tv, s);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd kernel launch");
+}
+
+ATTN_API attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                                    float descale_q, float descale_k, float descale_v,
+                                    int mask_kind, int window, const int* seqlens_k,
+                                    attn_stream_t stream) {
+    bool nothing = false;
+    attn_status_t st = check_fwd(q, k, v, o, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k,
+                                 &nothing);
+    if (st != ATTN_OK) return st;
+    if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports d = 128 only (d=%d)", d);
+    for (float f : {descale_q, descale_k, descale_v})
+        if (!(f > 0.f) || !std::isfinite(f))
+            return fail(ATTN_ERR_INVALID_ARG, "descale factors must be finite and > 0");
+    if (!std::isfinite(scale * descale_q * descale_k * 1.4426950408889634f))
+        return fail(ATTN_ERR_INVALID_ARG, "scale * descale_q * descale_k overflows FP32");
+    if (nothing) return ATTN_OK;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long rows = static_cast<long long>(B) * H * Nq;
+    if (Nk == 0) {
+        cudaError_t e = launch_fill_empty(o, lse, rows, d, true, s);
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fill kernel launch");
+    }
+    unsigned int* err = nullptr;
+    if ((st = err_word(&err)) != ATTN_OK) return st;
+    CUtensorMap tq, tk, tv;
+    const long long bh = static_cast<long long>(B) * H;
+    if ((st = encode_3d(&tq, q, d, Nq, bh, true)) != ATTN_OK) return st;
+    if ((st = encode_3d(&tk, k, d, Nk, bh, true)) != ATTN_OK) return st;
+    if ((st = encode_3d(&tv, v, d, Nk, bh, true)) != ATTN_OK) return st;
+    FwdArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k, err};
+    cudaError_t e = launch_fwd_fp8_maps(a, descale_q, descale_k, descale_v, tq, tk, tv, s);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd_fp8 kernel launch");
 }
 
 ATTN_API attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v, float* o,

@@ -1,4 +1,4 @@
-// fwd_sm103.cu -- BF16 fused attention forward on the sm_103a tensor cores.
+// fwd_sm103.cu -- fused attention forward (BF16 or E4M3 inputs) on the sm_103a tensor cores.
 //
 // The method is the query-tile online softmax of P2 ("Implement online
 // softmax for a whole tile of queries, not one query, and write the rescaling
@@ -47,6 +47,15 @@
 //     product of the first half runs while the second half is computed; then
 //     the epilogue O = A / l and lse.
 //   * m, l and A are FP32; P is rounded to BF16 for the P V product.
+//   * E4M3 variant (d = 128): Q, K and V are 8-bit floats with per-tensor
+//     dequantisation factors, the FP8 mode that P1 ("What did
+//     FlashAttention-2 and -3 change?") and P3 ("Where the merge is used
+//     today") credit to FlashAttention-3. Both products run as
+//     kind::f8f6f4 (K = 32 per instruction, half the MMA issue of BF16), P
+//     is rounded to E4M3 (P <= 2^8 < 448, the format's largest finite value)
+//     and stored four per tensor-memory column, the Q and K factors fold
+//     into the exp2 scale and V's into the final 1/l; m, l, A stay FP32 and
+//     O is BF16. Tiles are half the bytes, so the K and V rings are deeper.
 //   * Every mbarrier wait is bounded; on expiry the CTA records the site in
 //     the device error word, all roles stop, in-flight copies and MMAs are
 //     drained, tensor memory is freed and the kernel returns.
@@ -71,17 +80,28 @@ constexpr float kLn2 = 0.6931471805599453f;
 // when a block's max exceeds it by more than this (P stays <= 2^kTau = 256).
 constexpr float kTau = 8.0f;
 
-template <int D>
+// F8 = false: BF16 Q, K, V (kind::f16, K = 16 per MMA); F8 = true: E4M3
+// Q, K, V (kind::f8f6f4, K = 32 per MMA), d = 128 only.
+template <int D, bool F8>
 struct Cfg {
+    static constexpr int kElem = F8 ? 1 : 2;                   // bytes per element
+    static_assert((D * kElem) % 128 == 0, "head dim must fill 128-byte swizzle rows");
     // K/V ring depths: K is consumed one MMA step ahead of V, so it gets the
-    // deeper ring (Q 64 KiB + K 3 x 32 KiB + V 2 x 32 KiB = 224 KiB at d = 128).
-    static constexpr int kStagesK = (D == 64) ? 5 : 3;
-    static constexpr int kStagesV = (D == 64) ? 5 : 2;
+    // deeper ring (BF16, d = 128: Q 64 KiB + K 3 x 32 KiB + V 2 x 32 KiB =
+    // 224 KiB; E4M3: Q 32 KiB + K 4 x 16 KiB + V 4 x 16 KiB).
+    static constexpr int kStagesK = F8 ? 4 : (D == 64) ? 5 : 3;
+    static constexpr int kStagesV = F8 ? 4 : (D == 64) ? 5 : 2;
     static constexpr uint32_t kRowBytes = 128;                 // one swizzle atom row
-    static constexpr uint32_t kQTileBytes = BM * D * 2;
-    static constexpr uint32_t kKVBytes = BN * D * 2;
-    static constexpr uint32_t kQChunkBytes = BM * kRowBytes;   // 64 head dims of a Q tile
-    static constexpr uint32_t kKVChunkBytes = BN * kRowBytes;  // 64 head dims of a K/V block
+    static constexpr int kChunkElems = 128 / kElem;            // head dims per atom row
+    static constexpr int kChunks = D * kElem / 128;
+    static constexpr int kQKSteps = D * kElem / 32;            // MMAs of S = Q K^T (32 B of K each)
+    static constexpr int kPVKeys = 32 / kElem;                 // keys per P V MMA
+    static constexpr int kPVStepsHalf = (BN / 2) / kPVKeys;    // P V MMAs per 64-key half
+    static constexpr uint32_t kPHalfCols = (BN / 2) * kElem / 4;   // TMEM columns of half of P
+    static constexpr uint32_t kQTileBytes = BM * D * kElem;
+    static constexpr uint32_t kKVBytes = BN * D * kElem;
+    static constexpr uint32_t kQChunkBytes = BM * kRowBytes;   // one atom column of a Q tile
+    static constexpr uint32_t kKVChunkBytes = BN * kRowBytes;  // one atom column of a K/V block
     static constexpr uint32_t kQOff = 0;
     static constexpr uint32_t kKOff = kQOff + NT * kQTileBytes;
     static constexpr uint32_t kVOff = kKOff + kStagesK * kKVBytes;
@@ -130,14 +150,14 @@ __device__ __forceinline__ bool block_needs_mask(int kb, int row_first, int Lk, 
     return false;
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
-                 float* __restrict__ lse, int H, int Nq, int Nk, float scale_log2, int mask_kind,
-                 int window, const int* __restrict__ seqlens_k, unsigned int* __restrict__ err,
-                 int reverse_order) {
-    using C = Cfg<D>;
+                 float* __restrict__ lse, int H, int Nq, int Nk, float scale_log2, float o_mul,
+                 int mask_kind, int window, const int* __restrict__ seqlens_k,
+                 unsigned int* __restrict__ err, int reverse_order) {
+    using C = Cfg<D, F8>;
     constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -215,9 +235,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ptx::prefetch_tmap(&tm_q);
                     ptx::mbar_arrive_expect_tx(bar(C::bQFull), NT * C::kQTileBytes);
                     for (int t = 0; t < NT; ++t)
-                        for (int c = 0; c < D / 64; ++c)
+                        for (int c = 0; c < C::kChunks; ++c)
                             ptx::tma_load_3d(sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes,
-                                             &tm_q, bar(C::bQFull), c * 64, q0 + t * BM, bh);
+                                             &tm_q, bar(C::bQFull), c * C::kChunkElems, q0 + t * BM,
+                                             bh);
                 }
             }
             int issued = 0;
@@ -229,9 +250,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (!__all_sync(0xffffffffu, got)) break;
                 if (leader) {
                     ptx::mbar_arrive_expect_tx(bar(full0 + st), C::kKVBytes);
-                    for (int c = 0; c < D / 64; ++c)
+                    for (int c = 0; c < C::kChunks; ++c)
                         ptx::tma_load_3d(ring + st * C::kKVBytes + c * C::kKVChunkBytes, map,
-                                         bar(full0 + st), c * 64, s * BN, bh);
+                                         bar(full0 + st), c * C::kChunkElems, s * BN, bh);
                 }
                 __syncwarp();
                 issued = i + 1;
@@ -252,8 +273,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // operand descriptors stay warp-uniform.
         if (lo < hi) {
             const bool leader = ptx::elect_one();
-            constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(BM, D, true);
+            constexpr uint32_t kIdescS =
+                F8 ? ptx::idesc_e4m3_f32(BM, BN, false) : ptx::idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t kIdescPV =
+                F8 ? ptx::idesc_e4m3_f32(BM, D, true) : ptx::idesc_bf16_f32(BM, D, true);
             int p_seen[NT], pv_done[NT];
 #pragma unroll
             for (int t = 0; t < NT; ++t) { p_seen[t] = 0; pv_done[t] = 0; }
@@ -289,13 +312,18 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             ptx::tc_fence_after();
                             if (leader) {
 #pragma unroll
-                                for (int k4 = 0; k4 < BN / 32; ++k4) {
-                                    const int kk = half * (BN / 32) + k4;
+                                for (int k4 = 0; k4 < C::kPVStepsHalf; ++k4) {
+                                    const int kk = half * C::kPVStepsHalf + k4;
                                     const uint64_t bdesc = ptx::sdesc_sw128(
-                                        vbase + kk * 16 * C::kRowBytes, C::kKVChunkBytes, 1024);
-                                    ptx::mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                                                bdesc, kIdescPV,
-                                                (pv_done[t] > 0 || kk > 0) ? 1u : 0u);
+                                        vbase + kk * C::kPVKeys * C::kRowBytes, C::kKVChunkBytes,
+                                        1024);
+                                    const uint32_t acc = (pv_done[t] > 0 || kk > 0) ? 1u : 0u;
+                                    if constexpr (F8)
+                                        ptx::mma_ts_f8(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
+                                                       bdesc, kIdescPV, acc);
+                                    else
+                                        ptx::mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
+                                                    bdesc, kIdescPV, acc);
                                 }
                             }
                             __syncwarp();
@@ -319,13 +347,17 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const uint32_t kbase = sbase + C::kKOff + kst * C::kKVBytes;
                         if (leader) {
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
+                            for (int kk = 0; kk < C::kQKSteps; ++kk) {
                                 const uint32_t koff = (kk / 4) * C::kQChunkBytes + (kk % 4) * 32;
                                 const uint32_t boff = (kk / 4) * C::kKVChunkBytes + (kk % 4) * 32;
                                 const uint64_t adesc = ptx::sdesc_sw128(qbase + koff, 16, 1024);
                                 const uint64_t bdesc = ptx::sdesc_sw128(kbase + boff, 16, 1024);
-                                ptx::mma_ss(tmem + C::s_col(t), adesc, bdesc, kIdescS,
-                                            kk > 0 ? 1u : 0u);
+                                if constexpr (F8)
+                                    ptx::mma_ss_f8(tmem + C::s_col(t), adesc, bdesc, kIdescS,
+                                                   kk > 0 ? 1u : 0u);
+                                else
+                                    ptx::mma_ss(tmem + C::s_col(t), adesc, bdesc, kIdescS,
+                                                kk > 0 ? 1u : 0u);
                             }
                             ptx::mma_commit(bar(C::bSFull + t));
                         }
@@ -406,6 +438,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
+                // BF16: two stores of 16 columns (32 keys each) per half;
+                // E4M3: one store of 16 columns (64 keys) per half.
+                uint32_t pk8[16];
 #pragma unroll
                 for (int q4 = 0; q4 < 2; ++q4) {
                     uint32_t pk[16];
@@ -419,15 +454,22 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                 make_float2(__uint_as_float(sr[kk]), __uint_as_float(sr[kk + 1])),
                                 c2, nm2);
                             p[u] = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
-                            pk[kp + u] = pack_bf16x2(p[u].x, p[u].y);
+                            if constexpr (!F8) pk[kp + u] = pack_bf16x2(p[u].x, p[u].y);
+                        }
+                        if constexpr (F8) {
+                            pk8[q4 * 8 + kp / 2] = ptx::pack_e4m3x4(p[0].x, p[0].y, p[1].x, p[1].y);
+                            pk8[q4 * 8 + kp / 2 + 1] =
+                                ptx::pack_e4m3x4(p[2].x, p[2].y, p[3].x, p[3].y);
                         }
                         acc0 = __fadd2_rn(acc0, p[0]);
                         acc1 = __fadd2_rn(acc1, p[1]);
                         acc2 = __fadd2_rn(acc2, p[2]);
                         acc3 = __fadd2_rn(acc3, p[3]);
                     }
-                    ptx::tmem_st32x32b_x16(s_addr + half * (BN / 4) + q4 * 16, pk);
+                    if constexpr (!F8)
+                        ptx::tmem_st32x32b_x16(s_addr + half * C::kPHalfCols + q4 * 16, pk);
                 }
+                if constexpr (F8) ptx::tmem_st32x32b_x16(s_addr + half * C::kPHalfCols, pk8);
                 // Before the first P V product of this block: A <- diag(alpha) A,
                 // only for warps where some row moved its reference (rows that
                 // did not move multiply by exactly 1). Done here, after the
@@ -464,7 +506,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ptx::tc_fence_after();
         }
         const bool have = ok && c > 0;
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const float inv_l = (l > 0.f) ? o_mul / l : 0.f;
         __nv_bfloat16* orow = o + (static_cast<long long>(bh) * Nq + row) * D;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -500,16 +542,16 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                     const CUtensorMap& tv, cudaStream_t stream) {
-    using C = Cfg<D>;
+                     const CUtensorMap& tv, float scale_log2, float o_mul, cudaStream_t stream) {
+    using C = Cfg<D, F8>;
     static int configured_device = -1;   // attribute is per device; set once per device seen
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(fwd_sm103_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fwd_sm103_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
@@ -517,8 +559,8 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
     const int pairs = (a.Nq + BM * NT - 1) / (BM * NT);
     dim3 grid(pairs, a.H, a.B);
     const int reverse = (a.mask_kind & (kMaskCausal | kMaskWindow)) ? 1 : 0;
-    fwd_sm103_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(
-        tq, tk, tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.H, a.Nq, a.Nk, a.scale * kLog2e,
+    fwd_sm103_kernel<D, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(
+        tq, tk, tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.H, a.Nq, a.Nk, scale_log2, o_mul,
         a.mask_kind, a.window, a.seqlens_k, a.err, reverse);
     return cudaGetLastError();
 }
@@ -527,7 +569,18 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 
 cudaError_t launch_fwd_sm103_maps(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                   const CUtensorMap& tv, cudaStream_t stream) {
-    return a.d == 64 ? launch_d<64>(a, tq, tk, tv, stream) : launch_d<128>(a, tq, tk, tv, stream);
+    const float sl2 = a.scale * kLog2e;
+    return a.d == 64 ? launch_d<64, false>(a, tq, tk, tv, sl2, 1.f, stream)
+                     : launch_d<128, false>(a, tq, tk, tv, sl2, 1.f, stream);
+}
+
+// E4M3 inputs, d = 128: the score scale folds the Q and K dequantisation
+// factors, and the output multiplier is V's factor (O = descale_v A / l).
+cudaError_t launch_fwd_fp8_maps(const FwdArgs& a, float descale_q, float descale_k,
+                                float descale_v, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, cudaStream_t stream) {
+    const float sl2 = a.scale * descale_q * descale_k * kLog2e;
+    return launch_d<128, true>(a, tq, tk, tv, sl2, descale_v, stream);
 }
 
 }  // namespace attn

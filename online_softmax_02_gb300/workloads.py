@@ -24,9 +24,12 @@ figures they discuss):
                64 key splits.
   softmax      [4096, 32768] FP32 scores, N(0, 1): batches of long vectors
                as in the row-softmax measurements the pages quote.
+E4M3 variants of any workload (`generate_fp8`) draw the same FP32 values and
+store each of q, k, v as E4M3 with one power-of-two factor per tensor.
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 from dataclasses import dataclass, field
 
@@ -125,6 +128,30 @@ def generate(w: Workload):
         v = torch.randn(w.B, w.H, w.Nk, w.d, generator=g, dtype=torch.float32)
     q, k, v = (t.to(w.dtype).contiguous() for t in (q, k, v))
     return {"q": q, "k": k, "v": v, "seqlens_k": seqlens}
+
+
+E4M3_MAX = 448.0                         # largest finite E4M3 value
+
+
+def quantize_e4m3(t):
+    """Store a tensor as E4M3 with a per-tensor power-of-two factor:
+    returns (t8, descale) with t8 = round_e4m3(t / descale) and descale the
+    smallest power of two for which max|t| / descale <= 448. t8 * descale is
+    then exact in FP32, so both sides see the same real inputs."""
+    amax = float(t.abs().max())
+    descale = 2.0 ** math.ceil(math.log2(amax / E4M3_MAX)) if amax > 0 else 1.0
+    return (t.float() / descale).to(torch.float8_e4m3fn).contiguous(), descale
+
+
+def generate_fp8(w: Workload):
+    """The inputs of workload `w` (same seeded draws as `generate`, in FP32)
+    stored as E4M3: dict with q, k, v (float8_e4m3fn), descale_q/k/v, and
+    seqlens_k."""
+    x = generate(dataclasses.replace(w, dtype=torch.float32))
+    out = {"seqlens_k": x["seqlens_k"]}
+    for n in ("q", "k", "v"):
+        out[n], out["descale_" + n] = quantize_e4m3(x[n])
+    return out
 
 
 SOFTMAX_ROWS, SOFTMAX_N = 4096, 32768    # row softmax workload: [4096, 32768] FP32
