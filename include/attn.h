@@ -297,6 +297,19 @@ attn_status_t attn_softmax_rows(const void* x, void* y, float* lse, long long ro
 attn_status_t attn_check_device_error(attn_stream_t stream);
 
 /*
+ * attn_exp2_soft -- diagnostic: y[i] = 2^x[i] by the software exponential
+ * the forward kernels use for part of the attention weights (the partial
+ * move of exponentials from the special-function unit to the FMA units that
+ * P1, "What did FlashAttention-2 and -3 change?", attributes to
+ * FlashAttention-4): Cody-Waite reduction n = round(x), f = x - n, then a
+ * degree-3 minimax polynomial for 2^f (relative error <= 1.02e-4 for
+ * -126 <= x <= 127) and n added to the exponent. x <= -127 (and -inf)
+ * gives +0; -127 < x < -126 gives a denormal below 2^-126.
+ *   x, y    device FP32 [n], 4-byte aligned; n >= 0. Asynchronous on stream.
+ */
+attn_status_t attn_exp2_soft(const float* x, float* y, long long n, attn_stream_t stream);
+
+/*
  * attn_selftest_bounded_wait -- diagnostic: launch one CTA that waits on a
  * shared-memory barrier that nothing ever completes, with a limit of
  * `limit_cycles` SM clock cycles (1 .. 2^31). The wait must give up, record

@@ -79,6 +79,8 @@ def load():
     lib.attn_softmax_rows.restype = I
     lib.attn_check_device_error.argtypes = [P]
     lib.attn_check_device_error.restype = I
+    lib.attn_exp2_soft.argtypes = [P, P, ctypes.c_longlong, P]
+    lib.attn_exp2_soft.restype = I
     lib.attn_selftest_bounded_wait.argtypes = [ctypes.c_longlong, P]
     lib.attn_selftest_bounded_wait.restype = I
     lib.attn_last_error.argtypes = []
@@ -463,6 +465,19 @@ def attn_check_device_error(stream=None):
     import torch
     h = _stream_handle(stream, torch.cuda.current_device()) if stream is not None else None
     _check(load().attn_check_device_error(h))
+
+
+def attn_exp2_soft(x, y=None, stream=None):
+    """Diagnostic: 2^x of a contiguous FP32 CUDA tensor by the forward
+    kernels' software exponential (``attn_exp2_soft``)."""
+    import torch
+    _require(x, "x", torch.float32)
+    y = torch.empty_like(x) if y is None else y
+    _require(y, "y", torch.float32, x.device)
+    with torch.cuda.device(x.device):
+        st = load().attn_exp2_soft(_ptr(x), _ptr(y), x.numel(), _stream_handle(stream, x.device))
+    _check(st)
+    return y
 
 
 def attn_selftest_bounded_wait(limit_cycles: int, stream=None):

@@ -114,6 +114,15 @@ __global__ void fill_empty_kernel(void* o, float* lse, long long rows, int d, in
     }
 }
 
+__global__ void exp2_soft_kernel(const float* x, float* y, long long n) {
+    for (long long i = 2 * (blockIdx.x * (long long)blockDim.x + threadIdx.x); i < n;
+         i += 2 * (long long)gridDim.x * blockDim.x) {
+        const float2 r = soft_exp2x2(make_float2(x[i], i + 1 < n ? x[i + 1] : 0.f));
+        y[i] = r.x;
+        if (i + 1 < n) y[i + 1] = r.y;
+    }
+}
+
 __global__ void selftest_wait_kernel(unsigned int* err, long long limit) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ int abort_flag;
@@ -429,6 +438,20 @@ ATTN_API attn_status_t attn_check_device_error(attn_stream_t stream) {
         return fail(ATTN_ERR_TIMEOUT, "device wait gave up (site %u)", w >> 8);
     }
     return ATTN_OK;
+}
+
+ATTN_API attn_status_t attn_exp2_soft(const float* x, float* y, long long n,
+                                      attn_stream_t stream) {
+    if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "n must be >= 0");
+    if (n == 0) return ATTN_OK;
+    if (x == nullptr || y == nullptr) return fail(ATTN_ERR_INVALID_ARG, "x and y must not be NULL");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 3u)
+        return fail(ATTN_ERR_INVALID_ARG, "x and y must be 4-byte aligned");
+    const long long pairs = (n + 1) / 2;
+    const unsigned grid = static_cast<unsigned>(std::min<long long>((pairs + 255) / 256, 4096));
+    exp2_soft_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_exp2_soft kernel launch");
 }
 
 ATTN_API attn_status_t attn_selftest_bounded_wait(long long limit_cycles, attn_stream_t stream) {

@@ -46,6 +46,41 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Software 2^x for two values at once on the FMA pipe (the forward kernel
+// computes part of its exponentials this way so that they do not all queue
+// on the MUFU unit; the partial software exponential is the FlashAttention-4
+// device P1 mentions under "What did FlashAttention-2 and -3 change?").
+// Method: Cody-Waite range reduction for base 2 -- n = round(x) by adding
+// 1.5 * 2^23 (the sum's low mantissa bits hold n), f = x - n in [-1/2, 1/2]
+// -- then 2^f by the degree-3 polynomial 1 + c1 f + c2 f^2 + c3 f^3 whose
+// coefficients minimise the maximum relative error on [-1/2, 1/2] (fitted
+// by linear programming; relative error 1.02e-4, see exp2_poly_fit.py), and
+// 2^n applied by adding n to the exponent field. Inputs are clamped to
+// >= -127, and a result whose exponent field would fall below zero is
+// returned as +0: x <= -127 (and -inf) gives +0, -127 < x < -126 a denormal
+// below 2^-126.
+constexpr float kExp2C1 = 0.6932829022407532f;
+constexpr float kExp2C2 = 0.24221095442771912f;
+constexpr float kExp2C3 = 0.055008936673402786f;
+
+__device__ __forceinline__ float2 soft_exp2x2(float2 x) {
+    constexpr float kRound = 12582912.0f;                       // 1.5 * 2^23
+    x.x = fmaxf(x.x, -127.f);
+    x.y = fmaxf(x.y, -127.f);
+    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
+    const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));
+    const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);  // x - n, exact
+    float2 p = __ffma2_rn(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
+    p = __ffma2_rn(p, f, make_float2(kExp2C1, kExp2C1));
+    p = __ffma2_rn(p, f, make_float2(1.f, 1.f));
+    // exponent field += n (mod 2^32: the low 9 bits of t's pattern, shifted
+    // to bit 23, are n's two's complement there); a negative result -> +0.
+    const uint32_t e0 = __float_as_uint(p.x) + (__float_as_uint(t.x) << 23);
+    const uint32_t e1 = __float_as_uint(p.y) + (__float_as_uint(t.y) << 23);
+    return make_float2(__int_as_float(max(static_cast<int>(e0), 0)),
+                       __int_as_float(max(static_cast<int>(e1), 0)));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);

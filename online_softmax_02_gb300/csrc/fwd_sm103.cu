@@ -47,6 +47,9 @@
 //     product of the first half runs while the second half is computed; then
 //     the epilogue O = A / l and lse.
 //   * m, l and A are FP32; P is rounded to BF16 for the P V product.
+//   * Exponentials: ex2.approx on the MUFU unit, except (BF16) one pair in
+//     every 16, which runs as a polynomial on the FMA pipe (soft_exp2x2:
+//     relative error 1.02e-4, below P's BF16 rounding).
 //   * E4M3 variant (d = 128): Q, K and V are 8-bit floats with per-tensor
 //     dequantisation factors, the FP8 mode that P1 ("What did
 //     FlashAttention-2 and -3 change?") and P3 ("Where the merge is used
@@ -79,6 +82,24 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Lazy-rescale threshold in log2 units: the row's reference max moves only
 // when a block's max exceeds it by more than this (P stays <= 2^kTau = 256).
 constexpr float kTau = 8.0f;
+// Of every 16 pairs of exponentials of P, this many are computed in software
+// on the FMA pipe (soft_exp2x2) and the rest by ex2.approx on the MUFU unit,
+// spread evenly through the group. Measured on GB300 (prefill B1 H64 8192^2
+// d128): BF16 1390 / 1408 / 1354 / 1313 / 1241 TFLOP/s with 0 / 1 / 2 / 4 /
+// 8 pairs, E4M3 1756 / 1667 / 1622 / 1501 / 1352: the softmax phase is bound
+// by latency and issue slots, not by the MUFU unit's throughput.
+#ifndef ATTN_SOFT_EXP2_PAIRS_BF16
+#define ATTN_SOFT_EXP2_PAIRS_BF16 1
+#endif
+#ifndef ATTN_SOFT_EXP2_PAIRS_E4M3
+#define ATTN_SOFT_EXP2_PAIRS_E4M3 0
+#endif
+template <bool F8>
+__host__ __device__ constexpr bool soft_pair(int idx) {
+    constexpr int k = F8 ? ATTN_SOFT_EXP2_PAIRS_E4M3 : ATTN_SOFT_EXP2_PAIRS_BF16;
+    static_assert(k >= 0 && k <= 16, "pairs per group of 16");
+    return (idx * k) % 16 < k;
+}
 
 // F8 = false: BF16 Q, K, V (kind::f16, K = 16 per MMA); F8 = true: E4M3
 // Q, K, V (kind::f8f6f4, K = 32 per MMA), d = 128 only.
@@ -453,7 +474,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             const float2 x = __ffma2_rn(
                                 make_float2(__uint_as_float(sr[kk]), __uint_as_float(sr[kk + 1])),
                                 c2, nm2);
-                            p[u] = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+                            if (soft_pair<F8>(kp + u))
+                                p[u] = soft_exp2x2(x);
+                            else
+                                p[u] = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
                             if constexpr (!F8) pk[kp + u] = pack_bf16x2(p[u].x, p[u].y);
                         }
                         if constexpr (F8) {
