@@ -14,22 +14,36 @@
 //   bwd_prep_kernel   D_i and LSE_i * log2(e) per query row into the
 //                     workspace, rows padded to a multiple of 128 (padding
 //                     rows get LSE = +inf, D = 0, so they contribute P = 0).
-//   bwd_dkdv_kernel   keys outer: a CTA owns 128 keys of one (b, h); for each
-//                     128-query block it computes S^T = K Q^T and
-//                     dP^T = V dO^T into tensor memory, one thread per key
-//                     row turns them into P^T and dS^T (BF16, written back
-//                     into tensor memory), and dV += P^T dO, dK += dS^T Q
+//   bwd_dkdv_kernel   keys outer: a CTA owns 128 keys of one (b, h) and walks
+//                     the query blocks in units of 64 queries. Per unit:
+//                     S^T = K Q_u^T and dP^T = V dO_u^T (M = 128 keys, N = 64)
+//                     into one of two tensor-memory buffers; one thread per
+//                     key row turns them into P^T and dS^T (BF16, written back
+//                     into the buffer); dV += P^T dO_u and dK += dS^T Q_u
 //                     accumulate in tensor memory (A operand from TMEM).
-//   bwd_dq_kernel     queries outer: a CTA owns 128 queries; per 128-key
-//                     block S = Q K^T, dP = dO V^T, dS (BF16, TMEM), and
-//                     dQ += dS K in tensor memory.
+//   bwd_dq_kernel     queries outer: a CTA owns 128 queries; per unit of 64
+//                     keys S = Q K_u^T, dP = dO V_u^T, dS (BF16, TMEM), and
+//                     dQ += dS K_u in tensor memory.
 // dQ is recomputed in its own pass (S and dP twice) rather than accumulated
-// with atomics, because the 512 tensor-memory columns hold S^T, dP^T, dK and
-// dV of a key block (4 x 128 at d = 128) but no dQ tile beside them.
+// with atomics: tensor memory holds the dK/dV kernel's two unit buffers
+// (4 x 64 columns) and its dK and dV accumulators (2 x 128 at d = 128), and
+// no dQ tile beside them.
 //
-// Warp roles (192 threads): warps 0-3 one thread per row (TMEM lanes 0-127),
-// warp 4 TMA producer, warp 5 MMA issuer and TMEM owner; both run their loops
-// on the whole warp and issue from one elected lane. Every wait is bounded.
+// Pipelining. The two buffers let the MMA warp issue unit u's products while
+// the row warps work on unit u - 1; S and dP are committed separately, so
+// the row warps compute P as soon as S is done (while dP's product runs),
+// and in the dK/dV kernel dV's product is issued as soon as P^T is stored,
+// dK's once dS^T is. Row work goes 32 columns at a time with the block's LSE
+// and D read as 16-byte shared-memory vectors.
+// Measured on GB300 (B1 H64 8192^2 d128): with the element-wise work taken
+// out the two kernels are only 8 % faster, so the limit is the MMA issue
+// stream itself (waits between the single issuer's groups drain the short
+// tensor queue), not the softmax.
+//
+// Warp roles (192 threads with 4 row warps): the row warps hold one thread
+// per row (TMEM lanes 0-127), then the TMA producer warp and the MMA issuer /
+// TMEM owner warp; those two run their loops on the whole warp and issue
+// from one elected lane. Every wait is bounded.
 #include <climits>
 #include "common.cuh"
 
@@ -37,8 +51,18 @@ namespace attn {
 namespace {
 
 constexpr int BT = 128;                   // rows per tile (queries or keys)
-constexpr int kThreadsB = 192;
-constexpr int kProdWarp = 4, kMmaWarpB = 5;
+constexpr int BU = 64;                    // rows of the inner tile per pipeline unit
+// Row warps: 4 (one per TMEM lane quarter; measured fastest) or 8 (two per
+// quarter, each taking half of a unit's columns: 6 % slower, the eight
+// arrivals per hand-off cost more than the shorter row work saves).
+#ifndef ATTN_BWD_ROW_WARPS
+#define ATTN_BWD_ROW_WARPS 4
+#endif
+constexpr int kRowWarpsB = ATTN_BWD_ROW_WARPS;
+static_assert(kRowWarpsB == 4 || kRowWarpsB == 8, "4 or 8 row warps");
+constexpr int kQuartersPerWarp = (BU / 32) / (kRowWarpsB / 4);
+constexpr int kThreadsB = (kRowWarpsB + 2) * 32;
+constexpr int kProdWarp = kRowWarpsB, kMmaWarpB = kRowWarpsB + 1;
 constexpr int NSB = 2;                    // ring stages
 constexpr uint32_t kTmemColsB = 512;
 constexpr float kLog2eB = 1.4426950408889634f;
@@ -48,6 +72,7 @@ struct BCfg {
     static constexpr uint32_t kRowBytes = 128;
     static constexpr uint32_t kTileBytes = BT * D * 2;          // one 128-row tile
     static constexpr uint32_t kChunkBytes = BT * kRowBytes;     // 64 head dims of a tile
+    static constexpr uint32_t kUnitBytes = BU * kRowBytes;      // offset of the second half
 };
 
 // --- dK/dV kernel shared memory: K, V once; ring of {Q, dO, LSE2, D} ---
@@ -63,13 +88,20 @@ struct KVCfg : BCfg<D> {
     static constexpr uint32_t lse_off(int s) { return q_off(s) + 2 * B::kTileBytes; }
     static constexpr uint32_t dd_off(int s) { return lse_off(s) + BT * 4; }
     static constexpr uint32_t kBarOff = kRingOff + NSB * kStageBytes;
+    static constexpr int kBufs = 2;       // unit buffers in tensor memory
+    // per buffer: S^T done, dP^T done (MMA commits); P^T stored, dS^T stored
+    // (one arrival per row warp)
     static constexpr int bKV = 0, bInFull = 1, bInEmpty = 1 + NSB, bS = 1 + 2 * NSB,
-                         bP = bS + 1, bDone = bP + 1, kNumBars = bDone + 1;
+                         bDP = bS + kBufs, bP = bDP + kBufs, bDS = bP + kBufs,
+                         bDone = bDS + kBufs, kNumBars = bDone + 1;
     static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    // tensor memory columns
-    static constexpr uint32_t cST = 0, cDPT = 128, cDV = 256, cDK = 256 + D;
+    // tensor memory columns: two unit buffers {S^T, dP^T} of 64 columns each,
+    // then the dV and dK accumulators
+    static constexpr uint32_t cS(int b) { return 128u * b; }
+    static constexpr uint32_t cDP(int b) { return 128u * b + BU; }
+    static constexpr uint32_t cDV = 256, cDK = 256 + D;
 };
 
 // --- dQ kernel shared memory: Q, dO once; ring of {K, V} ---
@@ -82,13 +114,25 @@ struct QCfg : BCfg<D> {
     static constexpr uint32_t k_off(int s) { return kRingOff + s * 2 * B::kTileBytes; }
     static constexpr uint32_t v_off(int s) { return k_off(s) + B::kTileBytes; }
     static constexpr uint32_t kBarOff = kRingOff + NSB * 2 * B::kTileBytes;
+    static constexpr int kBufs = 2;       // unit buffers in tensor memory
+    // per buffer: S done, dP done (MMA commits); dS stored (row warps)
     static constexpr int bQ = 0, bKVFull = 1, bKVEmpty = 1 + NSB, bS = 1 + 2 * NSB,
-                         bP = bS + 1, bDone = bP + 1, kNumBars = bDone + 1;
+                         bDP = bS + kBufs, bP = bDP + kBufs, bDone = bP + kBufs,
+                         kNumBars = bDone + 1;
     static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static constexpr uint32_t cS = 0, cDP = 128, cDQ = 256;
+    static constexpr uint32_t cS(int b) { return 128u * b; }
+    static constexpr uint32_t cDP(int b) { return 128u * b + BU; }
+    static constexpr uint32_t cDQ = 128u * kBufs;
+    static_assert(cDQ + D <= kTmemColsB, "tensor memory budget");
 };
+
+// Column (within a unit buffer) of the BF16 operand for K-step kk (16 rows
+// of the unit's inner dimension): each row warp writes its 32 rows' packed
+// values (16 columns) at the start of its own 32 score columns, so the two
+// warps that share a lane quarter never write columns the other still reads.
+__host__ __device__ constexpr uint32_t a_col(int kk) { return (kk / 2) * 32 + (kk % 2) * 8; }
 
 __device__ __forceinline__ bool visible(int q, int key, int Lk, bool causal, bool windowed,
                                         int window) {
@@ -176,8 +220,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ptx::mbar_init(bar(C::bInFull + s), 1);
             ptx::mbar_init(bar(C::bInEmpty + s), 1);
         }
-        ptx::mbar_init(bar(C::bS), 1);
-        ptx::mbar_init(bar(C::bP), 4);
+        for (int u = 0; u < C::kBufs; ++u) {
+            ptx::mbar_init(bar(C::bS + u), 1);
+            ptx::mbar_init(bar(C::bDP + u), 1);
+            ptx::mbar_init(bar(C::bP + u), kRowWarpsB);   // one arrival per row warp
+            ptx::mbar_init(bar(C::bDS + u), kRowWarpsB);
+        }
         ptx::mbar_init(bar(C::bDone), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -238,58 +286,78 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp == kMmaWarpB) {
         if (nblk > 0) {
             const bool leader = ptx::elect_one();
-            constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BT, BT, false);
+            constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BT, BU, false);
             constexpr uint32_t kIdG = ptx::idesc_bf16_f32(BT, D, true);
             bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKV), 0, abort_flag, err, kSiteQFull));
-            for (int i = 0; ok && i < nblk; ++i) {
-                const int st = i % NSB;
-                const uint32_t ph = (i / NSB) & 1;
-                ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bInFull + st), ph, abort_flag, err,
-                                                          kSiteKFull));
-                if (!ok) break;
-                ptx::tc_fence_after();
-                if (leader) {
-                    // S^T = K Q^T and dP^T = V dO^T (M = keys, N = queries)
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                        ptx::mma_ss(tmem + C::cST, ptx::sdesc_sw128(sbase + C::kKOff + off, 16, 1024),
-                                    ptx::sdesc_sw128(sbase + C::q_off(st) + off, 16, 1024), kIdS,
-                                    kk > 0 ? 1u : 0u);
+            // Units u = 2 i + hh: query half hh of block i, tensor-memory
+            // buffer u % kBufs. Issue order S(0), S(1), G(0), S(2), G(1), ...:
+            // the products of unit u run while the row warps work on unit
+            // u - 1, and G(u - 1) (dV, dK) follows as soon as they are done.
+            const int nu = 2 * nblk;
+            constexpr int L = C::kBufs - 1;      // G(v) is issued after S(v + L)
+            for (int u = 0; ok && u < nu + L; ++u) {
+                if (u < nu) {
+                    const int i = u / 2, hh = u % 2, st = i % NSB, bf = u % C::kBufs;
+                    if (hh == 0) {
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bInFull + st), (i / NSB) & 1,
+                                                                  abort_flag, err, kSiteKFull));
+                        if (!ok) break;
+                        ptx::tc_fence_after();
                     }
+                    if (leader) {
+                        // S^T = K Q_hh^T and dP^T = V dO_hh^T (M = 128 keys, N = 64 queries)
+                        const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
+                        const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                        ptx::mma_ss(tmem + C::cDPT, ptx::sdesc_sw128(sbase + C::kVOff + off, 16, 1024),
-                                    ptx::sdesc_sw128(sbase + C::do_off(st) + off, 16, 1024), kIdS,
-                                    kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_sw128(sbase + C::kKOff + off, 16, 1024),
+                                        ptx::sdesc_sw128(qh + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(bar(C::bS + bf));
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_sw128(sbase + C::kVOff + off, 16, 1024),
+                                        ptx::sdesc_sw128(dh + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(bar(C::bDP + bf));
                     }
-                    ptx::mma_commit(bar(C::bS));
+                    __syncwarp();
                 }
-                __syncwarp();
-                ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bP), i & 1, abort_flag, err,
-                                                          kSitePFull));
-                if (!ok) break;
-                ptx::tc_fence_after();
-                if (leader) {
-                    // dV += P^T dO, dK += dS^T Q (A from TMEM, B MN-major, K = queries)
+                if (u >= L) {
+                    const int v = u - L, i = v / 2, hh = v % 2, st = i % NSB, bf = v % C::kBufs;
+                    const uint32_t vph = (v / C::kBufs) & 1;
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bP + bf), vph, abort_flag, err,
+                                                              kSitePFull));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
+                    const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
+                    if (leader) {
+                        // dV += P^T dO_hh (A from TMEM, B MN-major, K = 64 queries)
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk) {
-                        ptx::mma_ts(tmem + C::cDV, tmem + C::cST + kk * 8,
-                                    ptx::sdesc_sw128(sbase + C::do_off(st) + kk * 16 * C::kRowBytes,
-                                                     C::kChunkBytes, 1024),
-                                    kIdG, (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BU / 16; ++kk)
+                            ptx::mma_ts(tmem + C::cDV, tmem + C::cS(bf) + a_col(kk),
+                                        ptx::sdesc_sw128(dh + kk * 16 * C::kRowBytes, C::kChunkBytes, 1024),
+                                        kIdG, (v > 0 || kk > 0) ? 1u : 0u);
                     }
+                    __syncwarp();
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bDS + bf), vph, abort_flag, err,
+                                                              kSitePFull));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (leader) {
+                        // dK += dS^T Q_hh
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk) {
-                        ptx::mma_ts(tmem + C::cDK, tmem + C::cDPT + kk * 8,
-                                    ptx::sdesc_sw128(sbase + C::q_off(st) + kk * 16 * C::kRowBytes,
-                                                     C::kChunkBytes, 1024),
-                                    kIdG, (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BU / 16; ++kk)
+                            ptx::mma_ts(tmem + C::cDK, tmem + C::cDP(bf) + a_col(kk),
+                                        ptx::sdesc_sw128(qh + kk * 16 * C::kRowBytes, C::kChunkBytes, 1024),
+                                        kIdG, (v > 0 || kk > 0) ? 1u : 0u);
+                        if (hh == 1) ptx::mma_commit(bar(C::bInEmpty + st));
                     }
-                    ptx::mma_commit(bar(C::bInEmpty + st));
+                    __syncwarp();
                 }
-                __syncwarp();
             }
             if (leader) ptx::mma_commit(bar(C::bDone));
             __syncwarp();
@@ -297,52 +365,96 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     } else {
         // one thread per key row
-        const int r = warp * 32 + lane;
+        // warps w and w + 4 share TMEM lane quarter w % 4 (key rows); each
+        // takes half of a unit's 64 query columns and, at the end, one of
+        // the two accumulators (dV: warps 0-3, dK: warps 4-7)
+        const int part = warp / 4;
+        const int r = (warp % 4) * 32 + lane;
         const int key = kb + r;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t a_st = tmem + lane_base + C::cST;
-        const uint32_t a_dpt = tmem + lane_base + C::cDPT;
+        const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
         const float2 c2 = make_float2(scale_log2, scale_log2);
         bool ok = true;
-        for (int i = 0; i < nblk; ++i) {
-            const bool got = wait_bounded(bar(C::bS), i & 1, abort_flag, err, kSiteSFull);
+        for (int u = 0; u < 2 * nblk; ++u) {
+            const int i = u / 2, hh = u % 2, bf = u % C::kBufs;
+            const bool got = wait_bounded(bar(C::bS + bf), (u / C::kBufs) & 1, abort_flag, err,
+                                          kSiteSFull);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             ptx::tc_fence_after();
             const int st = i % NSB;
-            const float* lse2 = reinterpret_cast<const float*>(smem + C::lse_off(st));
-            const float* dd = reinterpret_cast<const float*>(smem + C::dd_off(st));
-            const int q0 = (ilo + i) * BT;
-            const bool full_vis = (kb + BT <= Lk) && (!causal || kb + BT - 1 <= q0) &&
-                                  (!windowed || kb > q0 + BT - 1 - window);
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sv[64], dpv[64];
-                ptx::tmem_ld32x32b_x64(a_st + half * 64, sv);
-                ptx::tmem_ld32x32b_x64(a_dpt + half * 64, dpv);
-                uint32_t pkp[32], pks[32];
+            const float* lse2 = reinterpret_cast<const float*>(smem + C::lse_off(st)) + hh * BU;
+            const float* dd = reinterpret_cast<const float*>(smem + C::dd_off(st)) + hh * BU;
+            const int qb = (ilo + i) * BT + hh * BU;               // first query of the unit
+            const bool full_vis = (kb + BT <= Lk) && (!causal || kb + BT - 1 <= qb) &&
+                                  (!windowed || kb > qb + BU - 1 - window);
+            const uint32_t a_st = tmem + lane_base + C::cS(bf);
+            const uint32_t a_dpt = tmem + lane_base + C::cDP(bf);
+            // Phase 1 (needs S^T): P^T = exp2(S^T c - lse2) for this warp's
+            // queries (quarters of 32; LSE as 16-byte shared-memory vectors),
+            // kept in FP32 for phase 2 and stored as BF16 into the first 16 of
+            // the quarter's own 32 score columns (a_col), then handed to the
+            // MMA warp so dV's product can start.
+            float2 pf[kQuartersPerWarp][16];
 #pragma unroll
-                for (int qq = 0; qq < 64; qq += 2) {
-                    const int ql = half * 64 + qq;
+            for (int k = 0; k < kQuartersPerWarp; ++k) {
+                const int qt = part * kQuartersPerWarp + k;
+                uint32_t sv[32];
+                ptx::tmem_ld32x32b_x32(a_st + qt * 32, sv);
+                float4 l4[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) l4[e] = reinterpret_cast<const float4*>(lse2)[qt * 8 + e];
+                uint32_t pkp[16];
+#pragma unroll
+                for (int qi = 0; qi < 32; qi += 2) {
+                    const float4 l = l4[qi / 4];
+                    const float2 nl = (qi & 2) ? make_float2(-l.z, -l.w) : make_float2(-l.x, -l.y);
                     const float2 x = __ffma2_rn(
-                        make_float2(__uint_as_float(sv[qq]), __uint_as_float(sv[qq + 1])), c2,
-                        make_float2(-lse2[ql], -lse2[ql + 1]));
+                        make_float2(__uint_as_float(sv[qi]), __uint_as_float(sv[qi + 1])), c2, nl);
                     float p0 = ptx::ex2(x.x), p1 = ptx::ex2(x.y);
                     if (!full_vis) {
-                        if (!visible(q0 + ql, key, Lk, causal, windowed, window)) p0 = 0.f;
-                        if (!visible(q0 + ql + 1, key, Lk, causal, windowed, window)) p1 = 0.f;
+                        const int qg = qb + qt * 32 + qi;
+                        if (!visible(qg, key, Lk, causal, windowed, window)) p0 = 0.f;
+                        if (!visible(qg + 1, key, Lk, causal, windowed, window)) p1 = 0.f;
                     }
-                    const float d0 = p0 * (__uint_as_float(dpv[qq]) - dd[ql]);
-                    const float d1 = p1 * (__uint_as_float(dpv[qq + 1]) - dd[ql + 1]);
-                    pkp[qq / 2] = pack_bf16x2(p0, p1);
-                    pks[qq / 2] = pack_bf16x2(d0, d1);
+                    pf[k][qi / 2] = make_float2(p0, p1);
+                    pkp[qi / 2] = pack_bf16x2(p0, p1);
                 }
-                ptx::tmem_st32x32b_x32(a_st + half * 32, pkp);
-                ptx::tmem_st32x32b_x32(a_dpt + half * 32, pks);
+                ptx::tmem_st32x32b_x16(a_st + qt * 32, pkp);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(C::bP));
+            if (lane == 0) ptx::mbar_arrive(bar(C::bP + bf));
+            // Phase 2 (needs dP^T): dS^T = P^T (dP^T - D), BF16 into the
+            // quarter's own dP^T columns, handed over for dK's product.
+            const bool gotdp = wait_bounded(bar(C::bDP + bf), (u / C::kBufs) & 1, abort_flag, err,
+                                            kSiteSFull);
+            if (!__all_sync(0xffffffffu, gotdp)) { ok = false; break; }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kQuartersPerWarp; ++k) {
+                const int qt = part * kQuartersPerWarp + k;
+                uint32_t dpv[32];
+                ptx::tmem_ld32x32b_x32(a_dpt + qt * 32, dpv);
+                float4 d4[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) d4[e] = reinterpret_cast<const float4*>(dd)[qt * 8 + e];
+                uint32_t pks[16];
+#pragma unroll
+                for (int qi = 0; qi < 32; qi += 2) {
+                    const float4 dv4 = d4[qi / 4];
+                    const float2 nd = (qi & 2) ? make_float2(-dv4.z, -dv4.w) : make_float2(-dv4.x, -dv4.y);
+                    const float2 ds = __fmul2_rn(
+                        pf[k][qi / 2],
+                        __fadd2_rn(make_float2(__uint_as_float(dpv[qi]), __uint_as_float(dpv[qi + 1])),
+                                   nd));
+                    pks[qi / 2] = pack_bf16x2(ds.x, ds.y);
+                }
+                ptx::tmem_st32x32b_x16(a_dpt + qt * 32, pks);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(C::bDS + bf));
         }
         if (ok && nblk > 0) {
             ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bDone), 0, abort_flag, err, kSiteODone));
@@ -351,7 +463,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const bool have = ok && nblk > 0;
         const long long orow = (static_cast<long long>(bh) * Nk + key) * D;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {            // 0: dV, 1: dK
+        for (int which = part; which < 2; which += kRowWarpsB / 4) {   // 0: dV, 1: dK
             const uint32_t a = tmem + lane_base + (which ? C::cDK : C::cDV);
             const float mul = which ? scale : 1.f;
             __nv_bfloat16* dst = (which ? dk : dv) + orow;
@@ -431,8 +543,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             ptx::mbar_init(bar(C::bKVFull + s), 1);
             ptx::mbar_init(bar(C::bKVEmpty + s), 1);
         }
-        ptx::mbar_init(bar(C::bS), 1);
-        ptx::mbar_init(bar(C::bP), 4);
+        for (int u = 0; u < C::kBufs; ++u) {
+            ptx::mbar_init(bar(C::bS + u), 1);
+            ptx::mbar_init(bar(C::bDP + u), 1);
+            ptx::mbar_init(bar(C::bP + u), kRowWarpsB);   // one arrival per row warp
+        }
         ptx::mbar_init(bar(C::bDone), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -490,51 +605,61 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     } else if (warp == kMmaWarpB) {
         if (nblk > 0) {
             const bool leader = ptx::elect_one();
-            constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BT, BT, false);
+            constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BT, BU, false);
             constexpr uint32_t kIdG = ptx::idesc_bf16_f32(BT, D, true);
             bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQ), 0, abort_flag, err, kSiteQFull));
-            for (int i = 0; ok && i < nblk; ++i) {
-                const int st = i % NSB;
-                const uint32_t ph = (i / NSB) & 1;
-                ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKVFull + st), ph, abort_flag, err,
-                                                          kSiteKFull));
-                if (!ok) break;
-                ptx::tc_fence_after();
-                if (leader) {
-                    // S = Q K^T, dP = dO V^T (M = queries, N = keys)
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                        ptx::mma_ss(tmem + C::cS, ptx::sdesc_sw128(sbase + C::kQOff + off, 16, 1024),
-                                    ptx::sdesc_sw128(sbase + C::k_off(st) + off, 16, 1024), kIdS,
-                                    kk > 0 ? 1u : 0u);
+            // Units u = 2 j + hh: key half hh of block j, buffer u % 2; issue
+            // order S(0), S(1), G(0), S(2), G(1), ... as in the dK/dV kernel.
+            const int nu = 2 * nblk;
+            constexpr int L = C::kBufs - 1;      // G(v) is issued after S(v + L)
+            for (int u = 0; ok && u < nu + L; ++u) {
+                if (u < nu) {
+                    const int j = u / 2, hh = u % 2, st = j % NSB, bf = u % C::kBufs;
+                    if (hh == 0) {
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKVFull + st), (j / NSB) & 1,
+                                                                  abort_flag, err, kSiteKFull));
+                        if (!ok) break;
+                        ptx::tc_fence_after();
                     }
+                    if (leader) {
+                        // S = Q K_hh^T, dP = dO V_hh^T (M = 128 queries, N = 64 keys)
+                        const uint32_t kh = sbase + C::k_off(st) + hh * C::kUnitBytes;
+                        const uint32_t vh = sbase + C::v_off(st) + hh * C::kUnitBytes;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                        ptx::mma_ss(tmem + C::cDP, ptx::sdesc_sw128(sbase + C::kDOOff + off, 16, 1024),
-                                    ptx::sdesc_sw128(sbase + C::v_off(st) + off, 16, 1024), kIdS,
-                                    kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_sw128(sbase + C::kQOff + off, 16, 1024),
+                                        ptx::sdesc_sw128(kh + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(bar(C::bS + bf));
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_sw128(sbase + C::kDOOff + off, 16, 1024),
+                                        ptx::sdesc_sw128(vh + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(bar(C::bDP + bf));
                     }
-                    ptx::mma_commit(bar(C::bS));
+                    __syncwarp();
                 }
-                __syncwarp();
-                ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bP), i & 1, abort_flag, err,
-                                                          kSitePFull));
-                if (!ok) break;
-                ptx::tc_fence_after();
-                if (leader) {
-                    // dQ += dS K (A = dS from TMEM, B = K MN-major, K = keys)
+                if (u >= L) {
+                    const int v = u - L, j = v / 2, hh = v % 2, st = j % NSB, bf = v % C::kBufs;
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bP + bf), (v / C::kBufs) & 1, abort_flag,
+                                                              err, kSitePFull));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (leader) {
+                        // dQ += dS K_hh (A = dS from TMEM, B = K MN-major, K = 64 keys)
+                        const uint32_t kh = sbase + C::k_off(st) + hh * C::kUnitBytes;
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk) {
-                        ptx::mma_ts(tmem + C::cDQ, tmem + C::cS + kk * 8,
-                                    ptx::sdesc_sw128(sbase + C::k_off(st) + kk * 16 * C::kRowBytes,
-                                                     C::kChunkBytes, 1024),
-                                    kIdG, (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BU / 16; ++kk)
+                            ptx::mma_ts(tmem + C::cDQ, tmem + C::cS(bf) + a_col(kk),
+                                        ptx::sdesc_sw128(kh + kk * 16 * C::kRowBytes, C::kChunkBytes, 1024),
+                                        kIdG, (v > 0 || kk > 0) ? 1u : 0u);
+                        if (hh == 1) ptx::mma_commit(bar(C::bKVEmpty + st));
                     }
-                    ptx::mma_commit(bar(C::bKVEmpty + st));
+                    __syncwarp();
                 }
-                __syncwarp();
             }
             if (leader) ptx::mma_commit(bar(C::bDone));
             __syncwarp();
@@ -542,11 +667,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
     } else {
         // one thread per query row
-        const int r = warp * 32 + lane;
+        // warps w and w + 4 share TMEM lane quarter w % 4 (query rows);
+        // each takes half of a unit's 64 key columns and half of dQ's columns
+        const int part = warp / 4;
+        const int r = (warp % 4) * 32 + lane;
         const int row = q0 + r;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t a_s = tmem + lane_base + C::cS;
-        const uint32_t a_dp = tmem + lane_base + C::cDP;
+        const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
         const long long wrow = static_cast<long long>(bh) * Nq_pad + row;
         const float lse2 = ws_lse2[wrow];
         const float drow = ws_dd[wrow];
@@ -554,39 +680,65 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const bool live = (lse2 != -INFINITY) && (lse2 != INFINITY);
         const float2 c2 = make_float2(scale_log2, scale_log2);
         const float2 nl2 = make_float2(live ? -lse2 : 0.f, live ? -lse2 : 0.f);
+        const float2 nd2 = make_float2(-drow, -drow);
         bool ok = true;
-        for (int i = 0; i < nblk; ++i) {
-            const bool got = wait_bounded(bar(C::bS), i & 1, abort_flag, err, kSiteSFull);
+        for (int u = 0; u < 2 * nblk; ++u) {
+            const int j = u / 2, hh = u % 2, bf = u % C::kBufs;
+            const bool got = wait_bounded(bar(C::bS + bf), (u / C::kBufs) & 1, abort_flag, err,
+                                          kSiteSFull);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             ptx::tc_fence_after();
-            const int k0 = (jlo + i) * BT;
-            const bool full_vis = (k0 + BT <= Lk) && (!causal || k0 + BT - 1 <= q0) &&
-                                  (!windowed || k0 > q0 + BT - 1 - window);
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sv[64], dpv[64];
-                ptx::tmem_ld32x32b_x64(a_s + half * 64, sv);
-                ptx::tmem_ld32x32b_x64(a_dp + half * 64, dpv);
-                uint32_t pks[32];
+            const int kb0 = (jlo + j) * BT + hh * BU;               // first key of the unit
+            const bool full_vis = (kb0 + BU <= Lk) && (!causal || kb0 + BU - 1 <= q0) &&
+                                  (!windowed || kb0 > q0 + BT - 1 - window);
+            const uint32_t a_s = tmem + lane_base + C::cS(bf);
+            const uint32_t a_dp = tmem + lane_base + C::cDP(bf);
+            // P for this warp's keys (quarters of 32) as soon as S is done,
+            // kept in FP32 while dP's product finishes; then dS = P (dP - D)
+            // in BF16 into the first 16 of the quarter's own 32 score columns.
+            float2 pf[kQuartersPerWarp][16];
 #pragma unroll
-                for (int kk = 0; kk < 64; kk += 2) {
+            for (int k = 0; k < kQuartersPerWarp; ++k) {
+                const int kt = part * kQuartersPerWarp + k;
+                uint32_t sv[32];
+                ptx::tmem_ld32x32b_x32(a_s + kt * 32, sv);
+#pragma unroll
+                for (int kk = 0; kk < 32; kk += 2) {
                     const float2 x = __ffma2_rn(
                         make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), c2, nl2);
                     float p0 = live ? ptx::ex2(x.x) : 0.f, p1 = live ? ptx::ex2(x.y) : 0.f;
                     if (!full_vis) {
-                        const int key = k0 + half * 64 + kk;
+                        const int key = kb0 + kt * 32 + kk;
                         if (!visible(row, key, Lk, causal, windowed, window)) p0 = 0.f;
                         if (!visible(row, key + 1, Lk, causal, windowed, window)) p1 = 0.f;
                     }
-                    pks[kk / 2] = pack_bf16x2(p0 * (__uint_as_float(dpv[kk]) - drow),
-                                              p1 * (__uint_as_float(dpv[kk + 1]) - drow));
+                    pf[k][kk / 2] = make_float2(p0, p1);
                 }
-                ptx::tmem_st32x32b_x32(a_s + half * 32, pks);
+            }
+            const bool gotdp = wait_bounded(bar(C::bDP + bf), (u / C::kBufs) & 1, abort_flag, err,
+                                            kSiteSFull);
+            if (!__all_sync(0xffffffffu, gotdp)) { ok = false; break; }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kQuartersPerWarp; ++k) {
+                const int kt = part * kQuartersPerWarp + k;
+                uint32_t dpv[32];
+                ptx::tmem_ld32x32b_x32(a_dp + kt * 32, dpv);
+                uint32_t pks[16];
+#pragma unroll
+                for (int kk = 0; kk < 32; kk += 2) {
+                    const float2 ds = __fmul2_rn(
+                        pf[k][kk / 2],
+                        __fadd2_rn(make_float2(__uint_as_float(dpv[kk]), __uint_as_float(dpv[kk + 1])),
+                                   nd2));
+                    pks[kk / 2] = pack_bf16x2(ds.x, ds.y);
+                }
+                ptx::tmem_st32x32b_x16(a_s + kt * 32, pks);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(C::bP));
+            if (lane == 0) ptx::mbar_arrive(bar(C::bP + bf));
         }
         if (ok && nblk > 0) {
             ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bDone), 0, abort_flag, err, kSiteODone));
@@ -594,8 +746,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         const bool have = ok && nblk > 0;
         __nv_bfloat16* dst = dq + (static_cast<long long>(bh) * Nq + row) * D;
+        constexpr int kChunksPerWarp = (D / 32) / (kRowWarpsB / 4);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = part * kChunksPerWarp; cc < (part + 1) * kChunksPerWarp; ++cc) {
             uint32_t v32[32];
             if (have) {
                 ptx::tmem_ld32x32b_x32(tmem + lane_base + C::cDQ + cc * 32, v32);
