@@ -54,15 +54,20 @@ NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
     # launch at the full bench workload, 1-pass ncu capture (profiles/
     # ncu_traffic_full_size.md); valid while the kernel source is unchanged.
-    "fwd_sm103.cu": {"sha256": "99b536f424a8e2839c22254126fc4572b6b233be423d49920443f8516f56a1e8",
-                     "bytes_per_launch": 403241984 + 114888704,
-                     "workload": "prefill_B1_H64_N8192_d128_bf16"},
-    "decode.cu": {"sha256": "1307a0be67d90977d4847a9f6c760c5b2d48dad081c5b803233a750d89e4f405",
-                  "bytes_per_launch": 2147748864 + 3136768,
-                  "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split kernel)"},
-    "softmax.cu": {"sha256": "9a40d74a21d385c58919240ac5c54e555e31ccc3e2bd568868bc0f51f562068d",
-                   "bytes_per_launch": 537604096 + 475967488,
-                   "workload": "softmax_rows_4096x32768_f32"},
+    "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": "5f7dbc02479d68572a9eeb0dfe047b9437102c65ef18295d3827e502a1688d99",
+                 "bytes_per_launch": 403545856 + 115181312,
+                 "workload": "prefill_B1_H64_N8192_d128_bf16"},
+    "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": "5f7dbc02479d68572a9eeb0dfe047b9437102c65ef18295d3827e502a1688d99",
+                 "bytes_per_launch": 201697024 + 101104896,
+                 "workload": "prefill_B1_H64_N8192_d128_e4m3"},
+    "decode": {"file": "decode.cu",
+               "sha256": "1307a0be67d90977d4847a9f6c760c5b2d48dad081c5b803233a750d89e4f405",
+               "bytes_per_launch": 2147748864 + 3136768,
+               "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split kernel)"},
+    "softmax": {"file": "softmax.cu",
+                "sha256": "9a40d74a21d385c58919240ac5c54e555e31ccc3e2bd568868bc0f51f562068d",
+                "bytes_per_launch": 537604096 + 475967488,
+                "workload": "softmax_rows_4096x32768_f32"},
 }
 
 
@@ -73,9 +78,9 @@ def kernel_sha(name):
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def traffic_for(name, units_scale=1.0):
-    rec = NCU_TRAFFIC.get(name)
-    if not rec or rec.get("sha256") != kernel_sha(name):
+def traffic_for(key, units_scale=1.0):
+    rec = NCU_TRAFFIC.get(key)
+    if not rec or rec.get("sha256") != kernel_sha(rec["file"]):
         return None
     return rec["bytes_per_launch"] * units_scale
 
@@ -272,7 +277,7 @@ def run_ours(args, rank, world, dist_on):
     roofline = {"bound": "tensor", "achieved": round(achieved, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": traffic_for("fwd_sm103.cu", w.H / W.PREFILL.H),
+                "traffic": traffic_for("fwd_bf16", w.H / W.PREFILL.H),
                 "peak_source": "%s bf16_tflops (burst) from MEASURED_PEAKS.json" % peak_src
                 if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
                 "kernel": "fwd_sm103_kernel<128>",
@@ -386,7 +391,8 @@ def run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result):
         "value": round(whole_job_rate(fl, world, args.steps, f_total) / 1e12, 2),
         "unit": "TFLOP/s", "gpu_launches_per_step": 1,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak8, 1),
-                     "unit": "TFLOP/s", "frac": round(achieved / peak8, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak8, 4),
+                     "traffic": traffic_for("fwd_e4m3", w.H / W.PREFILL.H),
                      "peak_note": "measured bf16 burst x 2 (nominal e4m3 / bf16 dense ratio)"}}
     del q, k, v, o, lse, x
     return run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
@@ -468,7 +474,7 @@ def run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result):
               "workspace_bytes_per_step": int(2 * ws.numel()),
               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                           "traffic": traffic_for("decode.cu", wd.Nk / W.DECODE.Nk),
+                           "traffic": traffic_for("decode", wd.Nk / W.DECODE.Nk),
                            "algorithmic_bytes_per_step": alg_bytes,
                            "note": "time is both launches (split + combine) per step"}}
     del qd, kd, vd, xd
@@ -505,7 +511,7 @@ def run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result):
                       "128 KiB, 512 threads per row)",
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                     "traffic": traffic_for("softmax.cu", x.shape[0] / W.SOFTMAX_ROWS)}}
+                     "traffic": traffic_for("softmax", x.shape[0] / W.SOFTMAX_ROWS)}}
     del x, y, lse
     if not args.no_naive:
         result["softmax"]["naive_attention_context"] = naive_attention_context(args, dev, stream,
