@@ -121,3 +121,56 @@ def test_decode_argument_errors(lib, kw, code):
                                  a["Nk"], a["d"], a["scale"], a["seqlens"], a["num_splits"],
                                  a["ws"], a["ws_bytes"], None)
     assert st == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), 2),
+    (dict(dq=0.0), 1),
+    (dict(dk=float("inf")), 1),
+    (dict(dv=-1.0), 1),
+    (dict(scale=1e30, dq=1e30), 1),
+    (dict(q=FAKE + 8), 1),
+    (dict(mask_kind=2, window=0), 1),
+])
+def test_fwd_fp8_argument_errors(lib, kw, code):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, H=2, Nq=16, Nk=16, d=128,
+             scale=0.125, dq=1.0, dk=1.0, dv=1.0, mask_kind=0, window=0, seqlens=None)
+    a.update(kw)
+    st = lib.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+                          a["Nk"], a["d"], a["scale"], a["dq"], a["dk"], a["dv"], a["mask_kind"],
+                          a["window"], a["seqlens"], None)
+    assert st == code
+    assert lib.attn_last_error() != b""
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(rows=-1), 1),
+    (dict(rows=1 << 31), 1),
+    (dict(n=0), 1),
+    (dict(dtype=7), 2),
+    (dict(x=None), 1),
+    (dict(x=FAKE + 2), 1),            # FP32 rows must be 4-byte aligned
+    (dict(y=FAKE + 1, dtype=1), 1),   # BF16 rows must be 2-byte aligned
+    (dict(lse=FAKE + 2), 1),
+])
+def test_softmax_rows_argument_errors(lib, kw, code):
+    a = dict(x=FAKE, y=FAKE, lse=None, rows=4, n=16, dtype=0)
+    a.update(kw)
+    assert lib.attn_softmax_rows(a["x"], a["y"], a["lse"], a["rows"], a["n"], a["dtype"],
+                                 None) == code
+
+
+def test_softmax_rows_and_exp2_empty_are_ok(lib):
+    assert lib.attn_softmax_rows(None, None, None, 0, 16, 0, None) == 0
+    assert lib.attn_exp2_soft(None, None, 0, None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), 1),
+    (dict(x=None), 1),
+    (dict(y=FAKE + 2), 1),
+])
+def test_exp2_soft_argument_errors(lib, kw, code):
+    a = dict(x=FAKE, y=FAKE, n=8)
+    a.update(kw)
+    assert lib.attn_exp2_soft(a["x"], a["y"], a["n"], None) == code

@@ -76,3 +76,17 @@ def test_two_rank_max_and_rate():
     assert out[0] == out[1] == 15.0
     # 2 ranks x 3 steps x 1e12 units in 15 ms
     assert bench.whole_job_rate(1e12, world, 3, out[0]) == pytest.approx(4e14)
+
+
+def test_traffic_records_follow_their_source_hash(monkeypatch):
+    import bench
+    for key, rec in bench.NCU_TRAFFIC.items():
+        assert rec["bytes_per_launch"] > 0 and rec["file"].endswith(".cu")
+        got = bench.traffic_for(key)
+        assert got in (None, rec["bytes_per_launch"])
+        if got is not None:
+            assert bench.traffic_for(key, 0.25) == rec["bytes_per_launch"] * 0.25
+    monkeypatch.setitem(bench.NCU_TRAFFIC, "fwd_bf16",
+                        dict(bench.NCU_TRAFFIC["fwd_bf16"], sha256="0" * 64))
+    assert bench.traffic_for("fwd_bf16") is None
+    assert bench.traffic_for("no such kernel") is None
