@@ -308,18 +308,22 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // S^T = K Q_hh^T and dP^T = V dO_hh^T (M = 128 keys, N = 64 queries)
                         const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
                         const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
+                        const uint64_t kd0 = ptx::sdesc_sw128(sbase + C::kKOff, 16, 1024);
+                        const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::kVOff, 16, 1024);
+                        const uint64_t qd0 = ptx::sdesc_sw128(qh, 16, 1024);
+                        const uint64_t dd0 = ptx::sdesc_sw128(dh, 16, 1024);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_sw128(sbase + C::kKOff + off, 16, 1024),
-                                        ptx::sdesc_sw128(qh + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_add(kd0, off), ptx::sdesc_add(qd0, off),
+                                        kIdS, kk > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(bar(C::bS + bf));
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_sw128(sbase + C::kVOff + off, 16, 1024),
-                                        ptx::sdesc_sw128(dh + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_add(vd0, off), ptx::sdesc_add(dd0, off),
+                                        kIdS, kk > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(bar(C::bDP + bf));
                     }
@@ -334,12 +338,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ptx::tc_fence_after();
                     const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
                     const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
+                    const uint64_t qg0 = ptx::sdesc_sw128(qh, C::kChunkBytes, 1024);
+                    const uint64_t dg0 = ptx::sdesc_sw128(dh, C::kChunkBytes, 1024);
                     if (leader) {
                         // dV += P^T dO_hh (A from TMEM, B MN-major, K = 64 queries)
 #pragma unroll
                         for (int kk = 0; kk < BU / 16; ++kk)
                             ptx::mma_ts(tmem + C::cDV, tmem + C::cS(bf) + a_col(kk),
-                                        ptx::sdesc_sw128(dh + kk * 16 * C::kRowBytes, C::kChunkBytes, 1024),
+                                        ptx::sdesc_add(dg0, kk * 16 * C::kRowBytes),
                                         kIdG, (v > 0 || kk > 0) ? 1u : 0u);
                     }
                     __syncwarp();
@@ -352,7 +358,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int kk = 0; kk < BU / 16; ++kk)
                             ptx::mma_ts(tmem + C::cDK, tmem + C::cDP(bf) + a_col(kk),
-                                        ptx::sdesc_sw128(qh + kk * 16 * C::kRowBytes, C::kChunkBytes, 1024),
+                                        ptx::sdesc_add(qg0, kk * 16 * C::kRowBytes),
                                         kIdG, (v > 0 || kk > 0) ? 1u : 0u);
                         if (hh == 1) ptx::mma_commit(bar(C::bInEmpty + st));
                     }
@@ -625,18 +631,22 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         // S = Q K_hh^T, dP = dO V_hh^T (M = 128 queries, N = 64 keys)
                         const uint32_t kh = sbase + C::k_off(st) + hh * C::kUnitBytes;
                         const uint32_t vh = sbase + C::v_off(st) + hh * C::kUnitBytes;
+                        const uint64_t qd0 = ptx::sdesc_sw128(sbase + C::kQOff, 16, 1024);
+                        const uint64_t od0 = ptx::sdesc_sw128(sbase + C::kDOOff, 16, 1024);
+                        const uint64_t kd0 = ptx::sdesc_sw128(kh, 16, 1024);
+                        const uint64_t vd0 = ptx::sdesc_sw128(vh, 16, 1024);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_sw128(sbase + C::kQOff + off, 16, 1024),
-                                        ptx::sdesc_sw128(kh + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_add(qd0, off), ptx::sdesc_add(kd0, off),
+                                        kIdS, kk > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(bar(C::bS + bf));
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_sw128(sbase + C::kDOOff + off, 16, 1024),
-                                        ptx::sdesc_sw128(vh + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_add(od0, off), ptx::sdesc_add(vd0, off),
+                                        kIdS, kk > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(bar(C::bDP + bf));
                     }
@@ -651,10 +661,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (leader) {
                         // dQ += dS K_hh (A = dS from TMEM, B = K MN-major, K = 64 keys)
                         const uint32_t kh = sbase + C::k_off(st) + hh * C::kUnitBytes;
+                        const uint64_t kg0 = ptx::sdesc_sw128(kh, C::kChunkBytes, 1024);
 #pragma unroll
                         for (int kk = 0; kk < BU / 16; ++kk)
                             ptx::mma_ts(tmem + C::cDQ, tmem + C::cS(bf) + a_col(kk),
-                                        ptx::sdesc_sw128(kh + kk * 16 * C::kRowBytes, C::kChunkBytes, 1024),
+                                        ptx::sdesc_add(kg0, kk * 16 * C::kRowBytes),
                                         kIdG, (v > 0 || kk > 0) ? 1u : 0u);
                         if (hh == 1) ptx::mma_commit(bar(C::bKVEmpty + st));
                     }

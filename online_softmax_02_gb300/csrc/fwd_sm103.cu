@@ -324,6 +324,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             v_ready = true;
                         }
                         const uint32_t vbase = sbase + C::kVOff + vst * C::kKVBytes;
+                        const uint64_t vdesc0 = ptx::sdesc_sw128(vbase, C::kKVChunkBytes, 1024);
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
                             ok = __all_sync(0xffffffffu,
@@ -335,9 +336,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                                 for (int k4 = 0; k4 < C::kPVStepsHalf; ++k4) {
                                     const int kk = half * C::kPVStepsHalf + k4;
-                                    const uint64_t bdesc = ptx::sdesc_sw128(
-                                        vbase + kk * C::kPVKeys * C::kRowBytes, C::kKVChunkBytes,
-                                        1024);
+                                    const uint64_t bdesc =
+                                        ptx::sdesc_add(vdesc0, kk * C::kPVKeys * C::kRowBytes);
                                     const uint32_t acc = (pv_done[t] > 0 || kk > 0) ? 1u : 0u;
                                     if constexpr (F8)
                                         ptx::mma_ts_f8(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
@@ -367,12 +367,14 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         const uint32_t qbase = sbase + C::kQOff + t * C::kQTileBytes;
                         const uint32_t kbase = sbase + C::kKOff + kst * C::kKVBytes;
                         if (leader) {
+                            const uint64_t adesc0 = ptx::sdesc_sw128(qbase, 16, 1024);
+                            const uint64_t bdesc0 = ptx::sdesc_sw128(kbase, 16, 1024);
 #pragma unroll
                             for (int kk = 0; kk < C::kQKSteps; ++kk) {
                                 const uint32_t koff = (kk / 4) * C::kQChunkBytes + (kk % 4) * 32;
                                 const uint32_t boff = (kk / 4) * C::kKVChunkBytes + (kk % 4) * 32;
-                                const uint64_t adesc = ptx::sdesc_sw128(qbase + koff, 16, 1024);
-                                const uint64_t bdesc = ptx::sdesc_sw128(kbase + boff, 16, 1024);
+                                const uint64_t adesc = ptx::sdesc_add(adesc0, koff);
+                                const uint64_t bdesc = ptx::sdesc_add(bdesc0, boff);
                                 if constexpr (F8)
                                     ptx::mma_ss_f8(tmem + C::s_col(t), adesc, bdesc, kIdescS,
                                                    kk > 0 ? 1u : 0u);

@@ -164,6 +164,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// The descriptor of the same layout starting `bytes` further on: only the
+// start-address field (bits 0-13, address >> 4) changes, and it does not
+// carry out for shared-memory addresses below 256 KiB.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+    return desc + (bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: FP32 accumulator (bits 4-5 = 1), A and
 // B BF16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B K-major or
 // MN-major (bit 16), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
