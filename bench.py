@@ -334,7 +334,7 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
     """The causal and split-KV decode workloads (sub-objects of the line)."""
     import online_softmax_02_gb300 as attn
     if args.only not in ("all", "causal"):
-        return run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result)
+        return run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result)
     # ---------------- causal workload
     wc = W.CAUSAL
     xc = W.generate(wc)
@@ -358,6 +358,35 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
                                     peaks["bf16_tflops"], 4)}
     del qc, kc, vc, oc, lc, xc
     result["causal"] = causal
+    return run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result)
+
+
+def run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result):
+    """Sliding window 1024 plus padding, B8 H16 4096^2 (reported, no target)."""
+    import online_softmax_02_gb300 as attn
+    if args.only not in ("all", "masked"):
+        return run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result)
+    wm = W.MASKED
+    xm = W.generate(wm)
+    qm, km, vm = (xm[n].to(dev) for n in ("q", "k", "v"))
+    sl = xm["seqlens_k"].to(dev)
+    om = torch.empty_like(qm)
+    lm = torch.empty(qm.shape[:3], dtype=torch.float32, device=dev)
+
+    def step_m():
+        attn.attn_fwd(qm, km, vm, o=om, lse=lm, mask_kind=wm.mask_kind, window=wm.window,
+                      seqlens_k=sl, stream=stream)
+
+    m_total, m_per = time_loop(step_m, args.steps, args.warmup, stream, dist_on)
+    attn.attn_check_device_error(stream)
+    m_total = max_over_ranks(m_total, dist_on)
+    flm = flops(wm, xm["seqlens_k"].numpy())
+    result["masked"] = {
+        "config": wm.describe(), "ms_per_step": round(m_total / args.steps, 4),
+        "value": round(flm * world * args.steps / (m_total * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "flop_count": "visible pairs only (window and padding)",
+        "frac_of_peak": round(flm / (statistics.mean(m_per) * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+    del qm, km, vm, om, lm, xm
     return run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result)
 
 
@@ -640,8 +669,8 @@ def main():
     # profiling helpers: run one section, or a reduced size of it
     ap.add_argument("--no-naive", action="store_true",
                     help="skip the naive (score matrix in HBM) attention context measurement")
-    ap.add_argument("--only", choices=["all", "prefill", "causal", "fp8", "backward", "decode",
-                                       "softmax"], default="all")
+    ap.add_argument("--only", choices=["all", "prefill", "causal", "masked", "fp8", "backward",
+                                       "decode", "softmax"], default="all")
     ap.add_argument("--heads", type=int, default=0, help="override H of the prefill workload")
     ap.add_argument("--decode-nk", type=int, default=0, help="override Nk of the decode workload")
     ap.add_argument("--softmax-rows", type=int, default=0,

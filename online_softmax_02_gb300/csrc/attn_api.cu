@@ -80,9 +80,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D tensor map over [B*H][rows][d] with 128-byte swizzle and a box of one
-// swizzle atom row (128 bytes: 64 BF16 or 128 8-bit head dims) x 128 rows x 1.
+// swizzle atom row (128 bytes: 64 BF16 or 128 8-bit head dims) x box_rows x 1.
 attn_status_t encode_3d(CUtensorMap* m, const void* ptr, int d, int rows, long long bh,
-                        bool one_byte) {
+                        bool one_byte, unsigned box_rows = 128) {
     auto fn = encode_fn();
     if (fn == nullptr) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
     const cuuint64_t esz = one_byte ? 1 : 2;
@@ -90,7 +90,7 @@ attn_status_t encode_3d(CUtensorMap* m, const void* ptr, int d, int rows, long l
                           static_cast<cuuint64_t>(bh)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz,
                              static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d) * esz};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), 128, 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, one_byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                     3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -390,16 +390,18 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
     }
     unsigned int* err = nullptr;
     if ((st = err_word(&err)) != ATTN_OK) return st;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tk64, tv64;
     if ((st = encode_bf16_3d(&tq, q, d, Nq, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tk, k, d, Nk, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tv, v, d, Nk, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tdo, dout, d, Nq, bh)) != ATTN_OK) return st;
+    if ((st = encode_3d(&tk64, k, d, Nk, bh, false, 64)) != ATTN_OK) return st;   // dQ kernel units
+    if ((st = encode_3d(&tv64, v, d, Nk, bh, false, 64)) != ATTN_OK) return st;
     float* ws_lse2 = static_cast<float*>(workspace);
     float* ws_dd = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_region(B, H, Nq));
     BwdArgs a{q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, mask_kind, window,
               seqlens_k, ws_lse2, ws_dd, err};
-    e = launch_bwd(a, tq, tk, tv, tdo, s);
+    e = launch_bwd(a, tq, tk, tv, tdo, tk64, tv64, s);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_bwd kernel launch");
 }
 

@@ -29,8 +29,9 @@
 // (4 x 64 columns) and its dK and dV accumulators (2 x 128 at d = 128), and
 // no dQ tile beside them.
 //
-// Pipelining. The two buffers let the MMA warp issue unit u's products while
-// the row warps work on unit u - 1; S and dP are committed separately, so
+// Pipelining. The unit buffers (two in the dK/dV kernel; three in the dQ
+// kernel, whose K and V arrive as 64-key units in a ring of four slots) let
+// the MMA warp issue the next units' products while the row warps work; S and dP are committed separately, so
 // the row warps compute P as soon as S is done (while dP's product runs),
 // and in the dK/dV kernel dV's product is issued as soon as P^T is stored,
 // dK's once dS^T is. Row work goes 32 columns at a time with the block's LSE
@@ -104,19 +105,23 @@ struct KVCfg : BCfg<D> {
     static constexpr uint32_t cDV = 256, cDK = 256 + D;
 };
 
-// --- dQ kernel shared memory: Q, dO once; ring of {K, V} ---
+// --- dQ kernel shared memory: Q, dO once; ring of 64-key units {K, V} ---
 template <int D>
 struct QCfg : BCfg<D> {
     using B = BCfg<D>;
+    static constexpr int NSU = 4;                                   // unit slots
+    static constexpr uint32_t kUChunkBytes = BU * B::kRowBytes;     // 64 head dims of a unit
+    static constexpr uint32_t kUTileBytes = BU * D * 2;             // one 64-key K (or V) unit
     static constexpr uint32_t kQOff = 0;
     static constexpr uint32_t kDOOff = B::kTileBytes;
     static constexpr uint32_t kRingOff = 2 * B::kTileBytes;
-    static constexpr uint32_t k_off(int s) { return kRingOff + s * 2 * B::kTileBytes; }
-    static constexpr uint32_t v_off(int s) { return k_off(s) + B::kTileBytes; }
-    static constexpr uint32_t kBarOff = kRingOff + NSB * 2 * B::kTileBytes;
-    static constexpr int kBufs = 2;       // unit buffers in tensor memory
-    // per buffer: S done, dP done (MMA commits); dS stored (row warps)
-    static constexpr int bQ = 0, bKVFull = 1, bKVEmpty = 1 + NSB, bS = 1 + 2 * NSB,
+    static constexpr uint32_t k_off(int s) { return kRingOff + s * 2 * kUTileBytes; }
+    static constexpr uint32_t v_off(int s) { return k_off(s) + kUTileBytes; }
+    static constexpr uint32_t kBarOff = kRingOff + NSU * 2 * kUTileBytes;
+    static constexpr int kBufs = 3;       // unit buffers in tensor memory
+    // per slot: unit loaded, unit released; per buffer: S done, dP done (MMA
+    // commits), dS stored (row warps)
+    static constexpr int bQ = 0, bUFull = 1, bUEmpty = 1 + NSU, bS = 1 + 2 * NSU,
                          bDP = bS + kBufs, bP = bDP + kBufs, bDone = bP + kBufs,
                          kNumBars = bDone + 1;
     static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
@@ -508,8 +513,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // ---------------------------------------------------------------- dQ
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
-bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k64,
+              const __grid_constant__ CUtensorMap tm_v64, const __grid_constant__ CUtensorMap tm_do,
               const float* __restrict__ ws_lse2, const float* __restrict__ ws_dd,
               __nv_bfloat16* __restrict__ dq, int H, int Nq, int Nk, int Nq_pad, float scale_log2,
               float scale, int mask_kind, int window, const int* __restrict__ seqlens_k,
@@ -545,9 +550,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(C::bQ), 1);
-        for (int s = 0; s < NSB; ++s) {
-            ptx::mbar_init(bar(C::bKVFull + s), 1);
-            ptx::mbar_init(bar(C::bKVEmpty + s), 1);
+        for (int s = 0; s < C::NSU; ++s) {
+            ptx::mbar_init(bar(C::bUFull + s), 1);
+            ptx::mbar_init(bar(C::bUEmpty + s), 1);
         }
         for (int u = 0; u < C::kBufs; ++u) {
             ptx::mbar_init(bar(C::bS + u), 1);
@@ -571,8 +576,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (nblk > 0) {
             const bool leader = ptx::elect_one();
             if (leader) {
-                ptx::prefetch_tmap(&tm_k);
-                ptx::prefetch_tmap(&tm_v);
+                ptx::prefetch_tmap(&tm_k64);
+                ptx::prefetch_tmap(&tm_v64);
                 ptx::mbar_arrive_expect_tx(bar(C::bQ), 2 * C::kTileBytes);
                 for (int c = 0; c < D / 64; ++c) {
                     ptx::tma_load_3d(sbase + C::kQOff + c * C::kChunkBytes, &tm_q, bar(C::bQ),
@@ -581,31 +586,33 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                      c * 64, q0, bh);
                 }
             }
+            // one 64-key unit {K, V} per slot; unit u covers keys
+            // [jlo * BT + 64 u, + 64)
             int issued = 0;
-            for (int i = 0; i < nblk; ++i) {
-                const int st = i % NSB;
-                const uint32_t ph = (i / NSB) & 1;
-                const bool got = wait_bounded(bar(C::bKVEmpty + st), ph ^ 1, abort_flag, err,
+            for (int u = 0; u < 2 * nblk; ++u) {
+                const int st = u % C::NSU;
+                const uint32_t ph = (u / C::NSU) & 1;
+                const bool got = wait_bounded(bar(C::bUEmpty + st), ph ^ 1, abort_flag, err,
                                               kSiteKEmpty);
                 if (!__all_sync(0xffffffffu, got)) break;
                 if (leader) {
-                    const int k0 = (jlo + i) * BT;
-                    ptx::mbar_arrive_expect_tx(bar(C::bKVFull + st), 2 * C::kTileBytes);
+                    const int k0 = jlo * BT + u * BU;
+                    ptx::mbar_arrive_expect_tx(bar(C::bUFull + st), 2 * C::kUTileBytes);
                     for (int c = 0; c < D / 64; ++c) {
-                        ptx::tma_load_3d(sbase + C::k_off(st) + c * C::kChunkBytes, &tm_k,
-                                         bar(C::bKVFull + st), c * 64, k0, bh);
-                        ptx::tma_load_3d(sbase + C::v_off(st) + c * C::kChunkBytes, &tm_v,
-                                         bar(C::bKVFull + st), c * 64, k0, bh);
+                        ptx::tma_load_3d(sbase + C::k_off(st) + c * C::kUChunkBytes, &tm_k64,
+                                         bar(C::bUFull + st), c * 64, k0, bh);
+                        ptx::tma_load_3d(sbase + C::v_off(st) + c * C::kUChunkBytes, &tm_v64,
+                                         bar(C::bUFull + st), c * 64, k0, bh);
                     }
                 }
                 __syncwarp();
-                issued = i + 1;
+                issued = u + 1;
             }
             if (*abort_flag && leader) {
                 wait_bounded(bar(C::bQ), 0, nullptr, err, kSiteDrain, kWaitLimitCycles / 8);
-                for (int i = max(0, issued - NSB); i < issued; ++i)
-                    wait_bounded(bar(C::bKVFull + i % NSB), (i / NSB) & 1, nullptr, err, kSiteDrain,
-                                 kWaitLimitCycles / 8);
+                for (int u = max(0, issued - C::NSU); u < issued; ++u)
+                    wait_bounded(bar(C::bUFull + u % C::NSU), (u / C::NSU) & 1, nullptr, err,
+                                 kSiteDrain, kWaitLimitCycles / 8);
             }
         }
     } else if (warp == kMmaWarpB) {
@@ -614,60 +621,60 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BT, BU, false);
             constexpr uint32_t kIdG = ptx::idesc_bf16_f32(BT, D, true);
             bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQ), 0, abort_flag, err, kSiteQFull));
-            // Units u = 2 j + hh: key half hh of block j, buffer u % 2; issue
-            // order S(0), S(1), G(0), S(2), G(1), ... as in the dK/dV kernel.
+            // Units u: keys [jlo * BT + 64 u, + 64), ring slot u % NSU, tensor-
+            // memory buffer u % kBufs. Issue order S(0), S(1), S(2), G(0),
+            // S(3), G(1), ...: the products run two units ahead of the row
+            // warps, and a slot is released once its unit's dQ product is done.
             const int nu = 2 * nblk;
             constexpr int L = C::kBufs - 1;      // G(v) is issued after S(v + L)
             for (int u = 0; ok && u < nu + L; ++u) {
                 if (u < nu) {
-                    const int j = u / 2, hh = u % 2, st = j % NSB, bf = u % C::kBufs;
-                    if (hh == 0) {
-                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKVFull + st), (j / NSB) & 1,
-                                                                  abort_flag, err, kSiteKFull));
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                    }
+                    const int st = u % C::NSU, bf = u % C::kBufs;
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bUFull + st), (u / C::NSU) & 1,
+                                                              abort_flag, err, kSiteKFull));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
                     if (leader) {
-                        // S = Q K_hh^T, dP = dO V_hh^T (M = 128 queries, N = 64 keys)
-                        const uint32_t kh = sbase + C::k_off(st) + hh * C::kUnitBytes;
-                        const uint32_t vh = sbase + C::v_off(st) + hh * C::kUnitBytes;
+                        // S = Q K_u^T, dP = dO V_u^T (M = 128 queries, N = 64 keys)
                         const uint64_t qd0 = ptx::sdesc_sw128(sbase + C::kQOff, 16, 1024);
                         const uint64_t od0 = ptx::sdesc_sw128(sbase + C::kDOOff, 16, 1024);
-                        const uint64_t kd0 = ptx::sdesc_sw128(kh, 16, 1024);
-                        const uint64_t vd0 = ptx::sdesc_sw128(vh, 16, 1024);
+                        const uint64_t kd0 = ptx::sdesc_sw128(sbase + C::k_off(st), 16, 1024);
+                        const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::v_off(st), 16, 1024);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_add(qd0, off), ptx::sdesc_add(kd0, off),
-                                        kIdS, kk > 0 ? 1u : 0u);
+                            const uint32_t aoff = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                            const uint32_t boff = (kk / 4) * C::kUChunkBytes + (kk % 4) * 32;
+                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_add(qd0, aoff),
+                                        ptx::sdesc_add(kd0, boff), kIdS, kk > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(bar(C::bS + bf));
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_add(od0, off), ptx::sdesc_add(vd0, off),
-                                        kIdS, kk > 0 ? 1u : 0u);
+                            const uint32_t aoff = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                            const uint32_t boff = (kk / 4) * C::kUChunkBytes + (kk % 4) * 32;
+                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_add(od0, aoff),
+                                        ptx::sdesc_add(vd0, boff), kIdS, kk > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(bar(C::bDP + bf));
                     }
                     __syncwarp();
                 }
                 if (u >= L) {
-                    const int v = u - L, j = v / 2, hh = v % 2, st = j % NSB, bf = v % C::kBufs;
+                    const int v = u - L, st = v % C::NSU, bf = v % C::kBufs;
                     ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bP + bf), (v / C::kBufs) & 1, abort_flag,
                                                               err, kSitePFull));
                     if (!ok) break;
                     ptx::tc_fence_after();
                     if (leader) {
-                        // dQ += dS K_hh (A = dS from TMEM, B = K MN-major, K = 64 keys)
-                        const uint32_t kh = sbase + C::k_off(st) + hh * C::kUnitBytes;
-                        const uint64_t kg0 = ptx::sdesc_sw128(kh, C::kChunkBytes, 1024);
+                        // dQ += dS K_u (A = dS from TMEM, B = K MN-major, K = 64 keys)
+                        const uint64_t kg0 =
+                            ptx::sdesc_sw128(sbase + C::k_off(st), C::kUChunkBytes, 1024);
 #pragma unroll
                         for (int kk = 0; kk < BU / 16; ++kk)
                             ptx::mma_ts(tmem + C::cDQ, tmem + C::cS(bf) + a_col(kk),
                                         ptx::sdesc_add(kg0, kk * 16 * C::kRowBytes),
                                         kIdG, (v > 0 || kk > 0) ? 1u : 0u);
-                        if (hh == 1) ptx::mma_commit(bar(C::bKVEmpty + st));
+                        ptx::mma_commit(bar(C::bUEmpty + st));
                     }
                     __syncwarp();
                 }
@@ -802,7 +809,8 @@ cudaError_t set_smem(K kernel, uint32_t bytes, int* configured) {
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
+                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,
+                         const CUtensorMap& tv64, cudaStream_t stream) {
     static int cfg_kv = -1, cfg_q = -1;
     cudaError_t e = set_smem(bwd_dkdv_kernel<D>, KVCfg<D>::kSmemBytes, &cfg_kv);
     if (e != cudaSuccess) return e;
@@ -825,7 +833,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     dim3 g2((a.Nq + BT - 1) / BT, a.H, a.B);
     bwd_dq_kernel<D><<<g2, kThreadsB, QCfg<D>::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, a.ws_lse2, a.ws_dd, static_cast<__nv_bfloat16*>(a.dq), a.H, a.Nq, a.Nk,
+        tq, tk64, tv64, tdo, a.ws_lse2, a.ws_dd, static_cast<__nv_bfloat16*>(a.dq), a.H, a.Nq, a.Nk,
         Nq_pad, scale_log2, a.scale, a.mask_kind, a.window, a.seqlens_k, a.err);
     return cudaGetLastError();
 }
@@ -833,9 +841,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
-    return a.d == 64 ? launch_bwd_d<64>(a, tq, tk, tv, tdo, stream)
-                     : launch_bwd_d<128>(a, tq, tk, tv, tdo, stream);
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,
+                       const CUtensorMap& tv64, cudaStream_t stream) {
+    return a.d == 64 ? launch_bwd_d<64>(a, tq, tk, tv, tdo, tk64, tv64, stream)
+                     : launch_bwd_d<128>(a, tq, tk, tv, tdo, tk64, tv64, stream);
 }
 
 }  // namespace attn

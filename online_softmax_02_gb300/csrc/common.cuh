@@ -132,7 +132,8 @@ struct BwdArgs {
     unsigned int* err;
 };
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream);
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,
+                       const CUtensorMap& tv64, cudaStream_t stream);
 cudaError_t launch_softmax_rows(const void* x, void* y, float* lse, long long rows, int n,
                                 bool bf16, cudaStream_t stream);
 cudaError_t launch_fill_empty(void* o, float* lse, long long rows, int d, bool bf16,
