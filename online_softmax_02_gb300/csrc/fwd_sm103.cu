@@ -109,9 +109,10 @@ struct Cfg {
     static_assert((D * kElem) % 128 == 0, "head dim must fill 128-byte swizzle rows");
     // K/V ring depths: K is consumed one MMA step ahead of V, so it gets the
     // deeper ring (BF16, d = 128: Q 64 KiB + K 3 x 32 KiB + V 2 x 32 KiB =
-    // 224 KiB; E4M3: Q 32 KiB + K 4 x 16 KiB + V 4 x 16 KiB).
-    static constexpr int kStagesK = F8 ? 4 : (D == 64) ? 5 : 3;
-    static constexpr int kStagesV = F8 ? 4 : (D == 64) ? 5 : 2;
+    // 224 KiB; E4M3: Q 32 KiB + K 6 x 16 KiB + V 5 x 16 KiB = 208 KiB, 1 %
+    // faster than 4 + 4 on the E4M3 prefill).
+    static constexpr int kStagesK = F8 ? 6 : (D == 64) ? 5 : 3;
+    static constexpr int kStagesV = F8 ? 5 : (D == 64) ? 5 : 2;
     static constexpr uint32_t kRowBytes = 128;                 // one swizzle atom row
     static constexpr int kChunkElems = 128 / kElem;            // head dims per atom row
     static constexpr int kChunks = D * kElem / 128;
