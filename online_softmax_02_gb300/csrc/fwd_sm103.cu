@@ -172,6 +172,9 @@ __device__ __forceinline__ bool block_needs_mask(int kb, int row_first, int Lk, 
     return false;
 }
 
+// 352 threads, one CTA per SM. The register file is split by sub-partition
+// (16,384 each) and three of the eleven warps share one, so a thread gets at
+// most 168 registers.
 template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
