@@ -105,22 +105,22 @@ struct KVCfg : BCfg<D> {
     static constexpr uint32_t cDV = 256, cDK = 256 + D;
 };
 
-// --- dQ kernel shared memory: Q, dO once; ring of 64-key units {K, V} ---
+// --- dQ kernel: Q and dO live in tensor memory; shared memory holds a ring
+// of 64-key units {K, V} ---
 template <int D>
 struct QCfg : BCfg<D> {
     using B = BCfg<D>;
-    static constexpr int NSU = 4;                                   // unit slots
+    static constexpr int NSU = 6;                                   // unit slots
     static constexpr uint32_t kUChunkBytes = BU * B::kRowBytes;     // 64 head dims of a unit
     static constexpr uint32_t kUTileBytes = BU * D * 2;             // one 64-key K (or V) unit
-    static constexpr uint32_t kQOff = 0;
-    static constexpr uint32_t kDOOff = B::kTileBytes;
-    static constexpr uint32_t kRingOff = 2 * B::kTileBytes;
+    static constexpr uint32_t kRingOff = 0;
     static constexpr uint32_t k_off(int s) { return kRingOff + s * 2 * kUTileBytes; }
     static constexpr uint32_t v_off(int s) { return k_off(s) + kUTileBytes; }
     static constexpr uint32_t kBarOff = kRingOff + NSU * 2 * kUTileBytes;
-    static constexpr int kBufs = 3;       // unit buffers in tensor memory
-    // per slot: unit loaded, unit released; per buffer: S done, dP done (MMA
-    // commits), dS stored (row warps)
+    static constexpr int kBufs = 2;       // unit buffers in tensor memory
+    // bQ: the row warps have stored Q and dO in tensor memory; per slot: unit
+    // loaded, unit released; per buffer: S done, dP done (MMA commits), dS
+    // stored (row warps)
     static constexpr int bQ = 0, bUFull = 1, bUEmpty = 1 + NSU, bS = 1 + 2 * NSU,
                          bDP = bS + kBufs, bP = bDP + kBufs, bDone = bP + kBufs,
                          kNumBars = bDone + 1;
@@ -130,7 +130,9 @@ struct QCfg : BCfg<D> {
     static constexpr uint32_t cS(int b) { return 128u * b; }
     static constexpr uint32_t cDP(int b) { return 128u * b + BU; }
     static constexpr uint32_t cDQ = 128u * kBufs;
-    static_assert(cDQ + D <= kTmemColsB, "tensor memory budget");
+    static constexpr uint32_t cQ = cDQ + D;           // Q rows, two BF16 per column
+    static constexpr uint32_t cDO = cQ + D / 2;       // dO rows
+    static_assert(cDO + D / 2 <= kTmemColsB, "tensor memory budget");
 };
 
 // Column (within a unit buffer) of the BF16 operand for K-step kk (16 rows
@@ -513,8 +515,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // ---------------------------------------------------------------- dQ
 template <int D>
 __global__ void __launch_bounds__(kThreadsB, 1)
-bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k64,
-              const __grid_constant__ CUtensorMap tm_v64, const __grid_constant__ CUtensorMap tm_do,
+bwd_dq_kernel(const __nv_bfloat16* __restrict__ qg, const __grid_constant__ CUtensorMap tm_k64,
+              const __grid_constant__ CUtensorMap tm_v64, const __nv_bfloat16* __restrict__ dog,
               const float* __restrict__ ws_lse2, const float* __restrict__ ws_dd,
               __nv_bfloat16* __restrict__ dq, int H, int Nq, int Nk, int Nq_pad, float scale_log2,
               float scale, int mask_kind, int window, const int* __restrict__ seqlens_k,
@@ -549,7 +551,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int nblk = jhi - jlo;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar(C::bQ), 1);
+        ptx::mbar_init(bar(C::bQ), kRowWarpsB);
         for (int s = 0; s < C::NSU; ++s) {
             ptx::mbar_init(bar(C::bUFull + s), 1);
             ptx::mbar_init(bar(C::bUEmpty + s), 1);
@@ -578,13 +580,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (leader) {
                 ptx::prefetch_tmap(&tm_k64);
                 ptx::prefetch_tmap(&tm_v64);
-                ptx::mbar_arrive_expect_tx(bar(C::bQ), 2 * C::kTileBytes);
-                for (int c = 0; c < D / 64; ++c) {
-                    ptx::tma_load_3d(sbase + C::kQOff + c * C::kChunkBytes, &tm_q, bar(C::bQ),
-                                     c * 64, q0, bh);
-                    ptx::tma_load_3d(sbase + C::kDOOff + c * C::kChunkBytes, &tm_do, bar(C::bQ),
-                                     c * 64, q0, bh);
-                }
             }
             // one 64-key unit {K, V} per slot; unit u covers keys
             // [jlo * BT + 64 u, + 64)
@@ -609,7 +604,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 issued = u + 1;
             }
             if (*abort_flag && leader) {
-                wait_bounded(bar(C::bQ), 0, nullptr, err, kSiteDrain, kWaitLimitCycles / 8);
                 for (int u = max(0, issued - C::NSU); u < issued; ++u)
                     wait_bounded(bar(C::bUFull + u % C::NSU), (u / C::NSU) & 1, nullptr, err,
                                  kSiteDrain, kWaitLimitCycles / 8);
@@ -621,6 +615,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             constexpr uint32_t kIdS = ptx::idesc_bf16_f32(BT, BU, false);
             constexpr uint32_t kIdG = ptx::idesc_bf16_f32(BT, D, true);
             bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQ), 0, abort_flag, err, kSiteQFull));
+            ptx::tc_fence_after();
             // Units u: keys [jlo * BT + 64 u, + 64), ring slot u % NSU, tensor-
             // memory buffer u % kBufs. Issue order S(0), S(1), S(2), G(0),
             // S(3), G(1), ...: the products run two units ahead of the row
@@ -635,24 +630,22 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     if (!ok) break;
                     ptx::tc_fence_after();
                     if (leader) {
-                        // S = Q K_u^T, dP = dO V_u^T (M = 128 queries, N = 64 keys)
-                        const uint64_t qd0 = ptx::sdesc_sw128(sbase + C::kQOff, 16, 1024);
-                        const uint64_t od0 = ptx::sdesc_sw128(sbase + C::kDOOff, 16, 1024);
+                        // S = Q K_u^T, dP = dO V_u^T (M = 128 queries, N = 64 keys);
+                        // A = Q or dO from tensor memory (8 columns per 16 head
+                        // dims), B = the K or V unit from shared memory
                         const uint64_t kd0 = ptx::sdesc_sw128(sbase + C::k_off(st), 16, 1024);
                         const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::v_off(st), 16, 1024);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t aoff = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
                             const uint32_t boff = (kk / 4) * C::kUChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_add(qd0, aoff),
+                            ptx::mma_ts(tmem + C::cS(bf), tmem + C::cQ + kk * 8,
                                         ptx::sdesc_add(kd0, boff), kIdS, kk > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(bar(C::bS + bf));
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t aoff = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
                             const uint32_t boff = (kk / 4) * C::kUChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_add(od0, aoff),
+                            ptx::mma_ts(tmem + C::cDP(bf), tmem + C::cDO + kk * 8,
                                         ptx::sdesc_add(vd0, boff), kIdS, kk > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(bar(C::bDP + bf));
@@ -691,13 +684,40 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int r = (warp % 4) * 32 + lane;
         const int row = q0 + r;
         const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+        {
+            // This CTA's Q and dO rows into tensor memory (lane = row), the A
+            // operands of S and dP; rows past Nq are zero. With eight row
+            // warps the two warps of a lane quarter split Q and dO.
+            const long long grow = (static_cast<long long>(bh) * Nq + row) * D;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                if (kRowWarpsB == 8 && which != part) continue;
+                const __nv_bfloat16* src = (which ? dog : qg) + grow;
+                uint32_t wv[D / 2];
+#pragma unroll
+                for (int e = 0; e < D / 8; ++e) {
+                    uint4 u4 = make_uint4(0, 0, 0, 0);
+                    if (row < Nq) u4 = reinterpret_cast<const uint4*>(src)[e];
+                    wv[4 * e] = u4.x; wv[4 * e + 1] = u4.y; wv[4 * e + 2] = u4.z; wv[4 * e + 3] = u4.w;
+                }
+                const uint32_t dst = tmem + lane_base + (which ? C::cDO : C::cQ);
+                if constexpr (D == 128) ptx::tmem_st32x32b_x64(dst, wv);
+                else ptx::tmem_st32x32b_x32(dst, wv);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(C::bQ));
+        }
         const long long wrow = static_cast<long long>(bh) * Nq_pad + row;
         const float lse2 = ws_lse2[wrow];
         const float drow = ws_dd[wrow];
         // a row that sees no key (lse = -inf) or lies past Nq (+inf) has P = 0
         const bool live = (lse2 != -INFINITY) && (lse2 != INFINITY);
         const float2 c2 = make_float2(scale_log2, scale_log2);
-        const float2 nl2 = make_float2(live ? -lse2 : 0.f, live ? -lse2 : 0.f);
+        // P = exp2(S c - lse2); a row that sees no key takes -inf here, so
+        // every exponential is 0 without a per-element select
+        const float2 nl2 = make_float2(live ? -lse2 : -INFINITY, live ? -lse2 : -INFINITY);
         const float2 nd2 = make_float2(-drow, -drow);
         bool ok = true;
         for (int u = 0; u < 2 * nblk; ++u) {
@@ -724,7 +744,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int kk = 0; kk < 32; kk += 2) {
                     const float2 x = __ffma2_rn(
                         make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), c2, nl2);
-                    float p0 = live ? ptx::ex2(x.x) : 0.f, p1 = live ? ptx::ex2(x.y) : 0.f;
+                    float p0 = ptx::ex2(x.x), p1 = ptx::ex2(x.y);
                     if (!full_vis) {
                         const int key = kb0 + kt * 32 + kk;
                         if (!visible(row, key, Lk, causal, windowed, window)) p0 = 0.f;
@@ -833,7 +853,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     dim3 g2((a.Nq + BT - 1) / BT, a.H, a.B);
     bwd_dq_kernel<D><<<g2, kThreadsB, QCfg<D>::kSmemBytes, stream>>>(
-        tq, tk64, tv64, tdo, a.ws_lse2, a.ws_dd, static_cast<__nv_bfloat16*>(a.dq), a.H, a.Nq, a.Nk,
+        static_cast<const __nv_bfloat16*>(a.q), tk64, tv64,
+        static_cast<const __nv_bfloat16*>(a.dout), a.ws_lse2, a.ws_dd, static_cast<__nv_bfloat16*>(a.dq), a.H, a.Nq, a.Nk,
         Nq_pad, scale_log2, a.scale, a.mask_kind, a.window, a.seqlens_k, a.err);
     return cudaGetLastError();
 }
