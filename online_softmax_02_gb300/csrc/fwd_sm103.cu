@@ -196,8 +196,20 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int pair = reverse_order ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
+    // Unmasked: the pairs of one head are adjacent (they share K and V in
+    // L2). Causal or windowed: the longest pairs of every head come first,
+    // so the last wave holds the shortest CTAs instead of one head's
+    // longest ones.
+    int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    if (reverse_order) {
+        const int nbh = gridDim.y * gridDim.z;
+        const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                               (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+        pair = static_cast<int>(gridDim.x - 1 - lin / nbh);
+        const int bhl = static_cast<int>(lin % nbh);
+        h = bhl % H;
+        b = bhl / H;
+    }
     const int bh = b * H + h;
     const int q0 = pair * (BM * NT);
 
