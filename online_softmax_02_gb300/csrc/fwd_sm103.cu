@@ -46,8 +46,10 @@
 //     row max (four independent three-input max chains) and row sum (packed
 //     FP32x2 adds) in registers -- no shuffles, the row is in one thread --,
 //     exp2 with the scale folded into one packed FMA, P stored back to tensor
-//     memory in two 64-key halves, each signalled separately so the PV
-//     product of the first half runs while the second half is computed; then
+//     memory in two 64-key halves and signalled once, after both (the MMA
+//     warp reaches a tile's P V product well after its P is ready, so a
+//     separate hand-off per half only adds a wait to the issue stream: one
+//     hand-off per tile measured 1.507 -> 1.439 ms on the prefill); then
 //     the epilogue O = A / l and lse.
 //   * m, l and A are FP32; P is rounded to BF16 for the P V product.
 //   * Exponentials: ex2.approx on the MUFU unit, except (BF16) one pair in
@@ -121,7 +123,7 @@ struct Cfg {
     static constexpr int kChunks = D * kElem / 128;
     static constexpr int kQKSteps = D * kElem / 32;            // MMAs of S = Q K^T (32 B of K each)
     static constexpr int kPVKeys = 32 / kElem;                 // keys per P V MMA
-    static constexpr int kPVStepsHalf = (BN / 2) / kPVKeys;    // P V MMAs per 64-key half
+    static constexpr int kPVSteps = BN / kPVKeys;               // P V MMAs per block
     static constexpr uint32_t kPHalfCols = (BN / 2) * kElem / 4;   // TMEM columns of half of P
     static constexpr uint32_t kQTileBytes = BM * D * kElem;
     static constexpr uint32_t kKVBytes = BN * D * kElem;
@@ -138,8 +140,8 @@ struct Cfg {
     static constexpr int bVFull = bKEmpty + kStagesK;
     static constexpr int bVEmpty = bVFull + kStagesV;
     static constexpr int bSFull = bVEmpty + kStagesV;
-    static constexpr int bPFull = bSFull + NT;         // [NT][2]: per tile, per key half
-    static constexpr int bODone = bPFull + 2 * NT;
+    static constexpr int bPFull = bSFull + NT;         // [NT]: P of the tile's block stored
+    static constexpr int bODone = bPFull + NT;
     static constexpr int bDrain = bODone + NT;
     static constexpr int kNumBars = bDrain + 1;
     static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;  // tmem base, abort flag
@@ -239,8 +241,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         for (int t = 0; t < NT; ++t) {
             ptx::mbar_init(bar(C::bSFull + t), 1);
-            ptx::mbar_init(bar(C::bPFull + 2 * t), 4);       // one arrival per softmax warp
-            ptx::mbar_init(bar(C::bPFull + 2 * t + 1), 4);
+            ptx::mbar_init(bar(C::bPFull + t), 4);           // one arrival per softmax warp
             ptx::mbar_init(bar(C::bODone + t), 1);
         }
         ptx::mbar_init(bar(C::bDrain), 1);
@@ -259,8 +260,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == kProducerWarp || warp == kProducerVWarp) {
         // ------------------------------------------------------ TMA producers
         // Warp 8 loads Q and streams K; warp 10 streams V. Each ring is
-        // refilled as soon as the MMA warp releases a slot. The whole warp
-        // runs the loop (uniform control flow); one elected lane issues.
+        // refilled as soon as a slot is released (by the softmax warp that
+        // sees the block's last S product complete). The whole warp runs the
+        // loop (uniform control flow); one elected lane issues.
         if (lo < hi) {
             const bool leader = ptx::elect_one();
             const bool is_k = (warp == kProducerWarp);
@@ -334,8 +336,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (s - 1 >= R[t].lo && s - 1 < R[t].hi) {
-                        // O_t (+)= P_t V_{s-1}, one 64-key half at a time as the
-                        // softmax hands each half of P over.
+                        // O_t (+)= P_t V_{s-1} once the softmax has stored P_t.
                         if (!v_ready) {
                             ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bVFull + vst), vph,
                                                                       abort_flag, err, kSiteVFull));
@@ -344,31 +345,25 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         }
                         const uint32_t vbase = sbase + C::kVOff + vst * C::kKVBytes;
                         const uint64_t vdesc0 = ptx::sdesc_sw128(vbase, C::kKVChunkBytes, 1024);
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            ok = __all_sync(0xffffffffu,
-                                            wait_bounded(bar(C::bPFull + 2 * t + half), p_seen[t] & 1,
-                                                         abort_flag, err, kSitePFull));
-                            if (!ok) break;
-                            ptx::tc_fence_after();
-                            if (leader) {
-#pragma unroll
-                                for (int k4 = 0; k4 < C::kPVStepsHalf; ++k4) {
-                                    const int kk = half * C::kPVStepsHalf + k4;
-                                    const uint64_t bdesc =
-                                        ptx::sdesc_add(vdesc0, kk * C::kPVKeys * C::kRowBytes);
-                                    const uint32_t acc = (pv_done[t] > 0 || kk > 0) ? 1u : 0u;
-                                    if constexpr (F8)
-                                        ptx::mma_ts_f8(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                                                       bdesc, kIdescPV, acc);
-                                    else
-                                        ptx::mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                                                    bdesc, kIdescPV, acc);
-                                }
-                            }
-                            __syncwarp();
-                        }
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + t), p_seen[t] & 1,
+                                                                  abort_flag, err, kSitePFull));
                         if (!ok) break;
+                        ptx::tc_fence_after();
+                        if (leader) {
+#pragma unroll
+                            for (int kk = 0; kk < C::kPVSteps; ++kk) {
+                                const uint64_t bdesc =
+                                    ptx::sdesc_add(vdesc0, kk * C::kPVKeys * C::kRowBytes);
+                                const uint32_t acc = (pv_done[t] > 0 || kk > 0) ? 1u : 0u;
+                                if constexpr (F8)
+                                    ptx::mma_ts_f8(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
+                                                   bdesc, kIdescPV, acc);
+                                else
+                                    ptx::mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
+                                                bdesc, kIdescPV, acc);
+                            }
+                        }
+                        __syncwarp();
                         ++p_seen[t];
                         ++pv_done[t];
                         if (s - 1 == R[t].hi - 1 && leader) ptx::mma_commit(bar(C::bODone + t));
@@ -414,11 +409,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKFull + kst), kph, abort_flag,
                                                               err, kSiteKFull));
                 if (!ok) break;
-                if (leader) {
-                    if (s - 1 >= lo) ptx::mma_commit(bar(C::bVEmpty + vst));
-                    if (s < hi) ptx::mma_commit(bar(C::bKEmpty + kst));
-                }
-                __syncwarp();
+                // K_s and V_{s-1} are released by the softmax (no commit here:
+                // each commit costs the issue stream a few hundred cycles).
             }
             // Every MMA issued above completes before tensor memory is freed.
             if (leader) ptx::mma_commit(bar(C::bDrain));
@@ -446,6 +438,18 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int j = Rt.lo; j < Rt.hi; ++j, ++c) {
             const bool got = wait_bounded(bar(C::bSFull + t), c & 1, abort_flag, err, kSiteSFull);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            // Release K_j and V_{j-1}. In issue order PV_0(j-1), S_0(j),
+            // PV_1(j-1), S_1(j), the last MMA of step j that reads either is
+            // the S product of the last tile covering block j (tile 1 on its
+            // range, tile 0 on the blocks before it: the ranges are contiguous
+            // and tile 1's ends last), and its completion implies every
+            // earlier one. Nobody waits for the last blocks' releases.
+            if (wq == 0 && lane == 0 &&
+                (t == NT - 1 || !(j >= R[NT - 1].lo && j < R[NT - 1].hi))) {
+                const int ii = j - lo;
+                ptx::mbar_arrive(bar(C::bKEmpty + ii % NSK));
+                if (ii > 0) ptx::mbar_arrive(bar(C::bVEmpty + (ii - 1) % NSV));
+            }
             ptx::tc_fence_after();
             uint32_t sr[BN];
             ptx::tmem_ld32x32b_x128(s_addr, sr);
@@ -474,8 +478,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const float m_next = need ? m_blk : m_use;
             const float m_ref = (m_next == -INFINITY) ? 0.f : m_next;   // the P2 guard
             const float alpha = need ? ptx::ex2(m_use - m_ref) : 1.f;
-            // P = exp2(S * scale * log2e - m_ref), one 64-key half at a time:
-            // BF16 pairs into tensor memory over S, then signal the MMA warp.
+            // P = exp2(S * scale * log2e - m_ref), one 64-key half at a time
+            // (fewer live registers): BF16 pairs into tensor memory over S.
             const float2 nm2 = make_float2(-m_ref, -m_ref);
             float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
 #pragma unroll
@@ -535,11 +539,12 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         ptx::tmem_st32x32b_x32(o_addr + cc * 32, ov);
                     }
                 }
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(C::bPFull + 2 * t + half));
             }
+            // both halves of P (and any rescale of A) stored: hand P over
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(C::bPFull + t));
             const float2 a01 = __fadd2_rn(acc0, acc1), a23 = __fadd2_rn(acc2, acc3);
             const float2 asum = __fadd2_rn(a01, a23);
             l = fmaf(l, alpha, asum.x + asum.y);
