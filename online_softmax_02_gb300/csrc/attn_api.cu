@@ -19,10 +19,11 @@
 namespace attn {
 
 cudaError_t launch_fwd_sm103_maps(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, cudaStream_t stream);
+                                  const CUtensorMap& tv, const CUtensorMap& to,
+                                  cudaStream_t stream);
 cudaError_t launch_fwd_fp8_maps(const FwdArgs& a, float descale_q, float descale_k,
                                 float descale_v, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, cudaStream_t stream);
+                                const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream);
 
 namespace {
 
@@ -186,13 +187,14 @@ ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, voi
     }
     unsigned int* err = nullptr;
     if ((st = err_word(&err)) != ATTN_OK) return st;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const long long bh = static_cast<long long>(B) * H;
     if ((st = encode_bf16_3d(&tq, q, d, Nq, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tk, k, d, Nk, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tv, v, d, Nk, bh)) != ATTN_OK) return st;
+    if ((st = encode_bf16_3d(&to, o, d, Nq, bh)) != ATTN_OK) return st;   // the epilogue's stores
     FwdArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k, err};
-    cudaError_t e = launch_fwd_sm103_maps(a, tq, tk, tv, s);
+    cudaError_t e = launch_fwd_sm103_maps(a, tq, tk, tv, to, s);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd kernel launch");
 }
 
@@ -222,13 +224,14 @@ ATTN_API attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v,
     }
     unsigned int* err = nullptr;
     if ((st = err_word(&err)) != ATTN_OK) return st;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const long long bh = static_cast<long long>(B) * H;
     if ((st = encode_3d(&tq, q, d, Nq, bh, true)) != ATTN_OK) return st;
     if ((st = encode_3d(&tk, k, d, Nk, bh, true)) != ATTN_OK) return st;
     if ((st = encode_3d(&tv, v, d, Nk, bh, true)) != ATTN_OK) return st;
+    if ((st = encode_bf16_3d(&to, o, d, Nq, bh)) != ATTN_OK) return st;   // BF16 output
     FwdArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k, err};
-    cudaError_t e = launch_fwd_fp8_maps(a, descale_q, descale_k, descale_v, tq, tk, tv, s);
+    cudaError_t e = launch_fwd_fp8_maps(a, descale_q, descale_k, descale_v, tq, tk, tv, to, s);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd_fp8 kernel launch");
 }
 

@@ -50,7 +50,8 @@
 //     warp reaches a tile's P V product well after its P is ready, so a
 //     separate hand-off per half only adds a wait to the issue stream: one
 //     hand-off per tile measured 1.507 -> 1.439 ms on the prefill); then
-//     the epilogue O = A / l and lse.
+//     the epilogue O = A / l and lse, O leaving (BF16 inputs) through the
+//     tile's dead Q buffer and a TMA store.
 //   * m, l and A are FP32; P is rounded to BF16 for the P V product.
 //   * Exponentials: ex2.approx on the MUFU unit, except (BF16) one pair in
 //     every 16, which runs as a polynomial on the FMA pipe (soft_exp2x2:
@@ -183,7 +184,8 @@ __device__ __forceinline__ bool block_needs_mask(int kb, int row_first, int Lk, 
 template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 __nv_bfloat16* __restrict__ o,
                  float* __restrict__ lse, int H, int Nq, int Nk, float scale_log2, float o_mul,
                  int mask_kind, int window, const int* __restrict__ seqlens_k,
                  unsigned int* __restrict__ err, int reverse_order) {
@@ -229,7 +231,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     if (hi == 0) lo = 0;
 
-    if (threadIdx.x == 0) {
+    // The Q tiles are the first thing the CTA needs and the longest load it
+    // waits for: the thread that sets up the barriers starts them before the
+    // tensor-memory allocation and the block-wide barrier.
+    if (warp == kProducerWarp && lane == 0) {
         ptx::mbar_init(bar(C::bQFull), 1);
         for (int s = 0; s < NSK; ++s) {
             ptx::mbar_init(bar(C::bKFull + s), 1);
@@ -247,6 +252,21 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         ptx::mbar_init(bar(C::bDrain), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
+        if (lo < hi) {
+            // Only tiles that see some key: an empty tile's buffer is written
+            // by its epilogue straight away and must not receive a late Q.
+            int nq = 0;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) nq += (R[t].lo < R[t].hi) ? 1 : 0;
+            ptx::prefetch_tmap(&tm_q);
+            ptx::mbar_arrive_expect_tx(bar(C::bQFull), nq * C::kQTileBytes);
+            for (int t = 0; t < NT; ++t) {
+                if (R[t].lo >= R[t].hi) continue;
+                for (int c = 0; c < C::kChunks; ++c)
+                    ptx::tma_load_3d(sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes,
+                                     &tm_q, bar(C::bQFull), c * C::kChunkElems, q0 + t * BM, bh);
+            }
+        }
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -259,7 +279,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (warp == kProducerWarp || warp == kProducerVWarp) {
         // ------------------------------------------------------ TMA producers
-        // Warp 8 loads Q and streams K; warp 10 streams V. Each ring is
+        // Warp 8 (which started the Q loads above) streams K; warp 10
+        // streams V. Each ring is
         // refilled as soon as a slot is released (by the softmax warp that
         // sees the block's last S product complete). The whole warp runs the
         // loop (uniform control flow); one elected lane issues.
@@ -271,18 +292,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int empty0 = is_k ? C::bKEmpty : C::bVEmpty;
             const uint32_t ring = sbase + (is_k ? C::kKOff : C::kVOff);
             const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-            if (leader) {
-                ptx::prefetch_tmap(map);
-                if (is_k) {
-                    ptx::prefetch_tmap(&tm_q);
-                    ptx::mbar_arrive_expect_tx(bar(C::bQFull), NT * C::kQTileBytes);
-                    for (int t = 0; t < NT; ++t)
-                        for (int c = 0; c < C::kChunks; ++c)
-                            ptx::tma_load_3d(sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes,
-                                             &tm_q, bar(C::bQFull), c * C::kChunkElems, q0 + t * BM,
-                                             bh);
-                }
-            }
+            if (leader) ptx::prefetch_tmap(map);
             int issued = 0;
             for (int s = lo; s < hi; ++s) {
                 const int i = s - lo, st = i % ns;
@@ -558,6 +568,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool have = ok && c > 0;
         const float inv_l = (l > 0.f) ? o_mul / l : 0.f;
         __nv_bfloat16* orow = o + (static_cast<long long>(bh) * Nq + row) * D;
+        // BF16 inputs: O_t goes through tile t's Q buffer (free once O_t is
+        // final: every S_t product was issued before the last P_t V one) in
+        // the 128-byte-swizzled layout Q arrived in -- 16-byte chunk j of row
+        // r at j ^ (r % 8), so a warp's stores hit every bank once per
+        // wavefront -- and leaves in one TMA store per 64 head dims. E4M3
+        // inputs (a Q tile of half the bytes) store rows directly.
+        const uint32_t obuf = sbase + C::kQOff + t * C::kQTileBytes;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t ov[32];
@@ -567,16 +584,35 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                 for (int e = 0; e < 32; ++e) ov[e] = 0u;
             }
-            if (row < Nq) {
-                uint32_t pw[16];
+            uint32_t pw[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pw[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l,
-                                        __uint_as_float(ov[2 * e + 1]) * inv_l);
+            for (int e = 0; e < 16; ++e)
+                pw[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l,
+                                    __uint_as_float(ov[2 * e + 1]) * inv_l);
+            if constexpr (!F8) {
+                const uint32_t rbase = obuf + (cc / 2) * C::kQChunkBytes + r * 128;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t j = (cc % 2) * 4 + e;
+                    ptx::st_shared_v4(rbase + ((j ^ (r & 7)) << 4), pw[4 * e], pw[4 * e + 1],
+                                      pw[4 * e + 2], pw[4 * e + 3]);
+                }
+            } else if (row < Nq) {
                 uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     dst[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+            }
+        }
+        if constexpr (!F8) {
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(1 + t, 4 * 32);                 // the tile's four warps
+            if (wq == 0 && lane == 0 && row_first < Nq) {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_store_3d(&tm_o, obuf + c * C::kQChunkBytes, c * 64, row_first, bh);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_read_all();       // the buffer outlives the copy's reads
             }
         }
         if (lse != nullptr && row < Nq)
@@ -594,7 +630,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
 template <int D, bool F8>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                     const CUtensorMap& tv, float scale_log2, float o_mul, cudaStream_t stream) {
+                     const CUtensorMap& tv, const CUtensorMap& to, float scale_log2, float o_mul,
+                     cudaStream_t stream) {
     using C = Cfg<D, F8>;
     static int configured_device = -1;   // attribute is per device; set once per device seen
     int dev = 0;
@@ -610,7 +647,7 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
     dim3 grid(pairs, a.H, a.B);
     const int reverse = (a.mask_kind & (kMaskCausal | kMaskWindow)) ? 1 : 0;
     fwd_sm103_kernel<D, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(
-        tq, tk, tv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.H, a.Nq, a.Nk, scale_log2, o_mul,
+        tq, tk, tv, to, static_cast<__nv_bfloat16*>(a.o), a.lse, a.H, a.Nq, a.Nk, scale_log2, o_mul,
         a.mask_kind, a.window, a.seqlens_k, a.err, reverse);
     return cudaGetLastError();
 }
@@ -618,19 +655,21 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
 }  // namespace
 
 cudaError_t launch_fwd_sm103_maps(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, cudaStream_t stream) {
+                                  const CUtensorMap& tv, const CUtensorMap& to,
+                                  cudaStream_t stream) {
     const float sl2 = a.scale * kLog2e;
-    return a.d == 64 ? launch_d<64, false>(a, tq, tk, tv, sl2, 1.f, stream)
-                     : launch_d<128, false>(a, tq, tk, tv, sl2, 1.f, stream);
+    return a.d == 64 ? launch_d<64, false>(a, tq, tk, tv, to, sl2, 1.f, stream)
+                     : launch_d<128, false>(a, tq, tk, tv, to, sl2, 1.f, stream);
 }
 
 // E4M3 inputs, d = 128: the score scale folds the Q and K dequantisation
 // factors, and the output multiplier is V's factor (O = descale_v A / l).
 cudaError_t launch_fwd_fp8_maps(const FwdArgs& a, float descale_q, float descale_k,
                                 float descale_v, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, cudaStream_t stream) {
+                                const CUtensorMap& tv, const CUtensorMap& to,
+                                cudaStream_t stream) {
     const float sl2 = a.scale * descale_q * descale_k * kLog2e;
-    return launch_d<128, true>(a, tq, tk, tv, sl2, descale_v, stream);
+    return launch_d<128, true>(a, tq, tk, tv, to, sl2, descale_v, stream);
 }
 
 }  // namespace attn
