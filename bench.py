@@ -665,7 +665,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds-per-step", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-chunks", type=int, default=8, help="head groups of the e2e pipeline")
+    ap.add_argument("--e2e-chunks", type=int, default=16, help="head groups of the e2e pipeline")
     # profiling helpers: run one section, or a reduced size of it
     ap.add_argument("--no-naive", action="store_true",
                     help="skip the naive (score matrix in HBM) attention context measurement")

@@ -1,7 +1,8 @@
 """Long, large and degenerate cases against the FP64 oracle (GPU only):
 131072 keys through the forward kernel, a 32K-token causal head on sampled
 rows, many small heads, decode with one key per split and the split limit,
-one-element softmax rows, and one-key / one-query E4M3 problems."""
+one-element softmax rows, one-key / one-query E4M3 problems, and query
+tiles that see no key beside tiles that do."""
 import math
 
 import numpy as np
@@ -89,3 +90,24 @@ def test_fp8_degenerate_shapes(cuda_lib, orc, nq, nk):
     import test_gpu_fp8 as F8
     x = F8._fp8_inputs(1, 2, nq, nk, seed=nq * 1000 + nk)
     F8._compare(cuda_lib, orc, x, what=str((nq, nk)))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_empty_second_tile(cuda_lib, orc, d):
+    """A window of one key with short key lengths: in each 256-row pair of
+    query tiles the first tile has visible keys and the second has none, so
+    the second tile's output buffer is written while the first tile still
+    computes. Rows without a key must come out exactly 0 with lse = -inf."""
+    x = W.random_inputs(2, 3, 256, 256, d, seed=35 + d)
+    x["seqlens_k"] = torch.tensor([100, 60], dtype=torch.int32)
+    dev = torch.device("cuda:0")
+    o, lse = cuda_lib.attn_fwd(*(x[n].to(dev) for n in "qkv"), mask_kind=W.MASK_WINDOW | W.MASK_PADDING,
+                               window=1, seqlens_k=x["seqlens_k"].to(dev))
+    cuda_lib.attn_check_device_error()
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    ro, rl = orc.attention(*(x[n].float().numpy() for n in "qkv"), 1 / math.sqrt(d),
+                           W.MASK_WINDOW | W.MASK_PADDING, 1, x["seqlens_k"].numpy())
+    empty = np.isneginf(rl)
+    assert empty[:, :, 128:].all() and (~empty[:, :, :60]).all()
+    assert np.all(o[empty] == 0.0)
+    _check(o, lse, ro, rl)
