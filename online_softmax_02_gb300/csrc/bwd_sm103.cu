@@ -617,9 +617,9 @@ bwd_dq_kernel(const __nv_bfloat16* __restrict__ qg, const __grid_constant__ CUte
             bool ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQ), 0, abort_flag, err, kSiteQFull));
             ptx::tc_fence_after();
             // Units u: keys [jlo * BT + 64 u, + 64), ring slot u % NSU, tensor-
-            // memory buffer u % kBufs. Issue order S(0), S(1), S(2), G(0),
-            // S(3), G(1), ...: the products run two units ahead of the row
-            // warps, and a slot is released once its unit's dQ product is done.
+            // memory buffer u % kBufs. Issue order S(0), S(1), G(0), S(2),
+            // G(1), ...: the products run one unit ahead of the row warps;
+            // the row warps release a unit's K/V slot (below).
             const int nu = 2 * nblk;
             constexpr int L = C::kBufs - 1;      // G(v) is issued after S(v + L)
             for (int u = 0; ok && u < nu + L; ++u) {
@@ -667,7 +667,6 @@ bwd_dq_kernel(const __nv_bfloat16* __restrict__ qg, const __grid_constant__ CUte
                             ptx::mma_ts(tmem + C::cDQ, tmem + C::cS(bf) + a_col(kk),
                                         ptx::sdesc_add(kg0, kk * 16 * C::kRowBytes),
                                         kIdG, (v > 0 || kk > 0) ? 1u : 0u);
-                        ptx::mma_commit(bar(C::bUEmpty + st));
                     }
                     __syncwarp();
                 }
@@ -725,6 +724,11 @@ bwd_dq_kernel(const __nv_bfloat16* __restrict__ qg, const __grid_constant__ CUte
             const bool got = wait_bounded(bar(C::bS + bf), (u / C::kBufs) & 1, abort_flag, err,
                                           kSiteSFull);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            // S(u) complete implies dQ(u - 2) complete (issue order S(u - 1),
+            // dP(u - 1), dQ(u - 2), S(u), ...), so unit u - 2's K/V slot is
+            // free: released here rather than by a commit in the MMA stream.
+            if (warp == 0 && lane == 0 && u >= C::kBufs)
+                ptx::mbar_arrive(bar(C::bUEmpty + (u - C::kBufs) % C::NSU));
             ptx::tc_fence_after();
             const int kb0 = (jlo + j) * BT + hh * BU;               // first key of the unit
             const bool full_vis = (kb0 + BU <= Lk) && (!causal || kb0 + BU - 1 <= q0) &&
