@@ -185,7 +185,6 @@ template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                 __nv_bfloat16* __restrict__ o,
                  float* __restrict__ lse, int H, int Nq, int Nk, float scale_log2, float o_mul,
                  int mask_kind, int window, const int* __restrict__ seqlens_k,
                  unsigned int* __restrict__ err, int reverse_order) {
@@ -567,14 +566,18 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         const bool have = ok && c > 0;
         const float inv_l = (l > 0.f) ? o_mul / l : 0.f;
-        __nv_bfloat16* orow = o + (static_cast<long long>(bh) * Nq + row) * D;
-        // BF16 inputs: O_t goes through tile t's Q buffer (free once O_t is
-        // final: every S_t product was issued before the last P_t V one) in
-        // the 128-byte-swizzled layout Q arrived in -- 16-byte chunk j of row
-        // r at j ^ (r % 8), so a warp's stores hit every bank once per
-        // wavefront -- and leaves in one TMA store per 64 head dims. E4M3
-        // inputs (a Q tile of half the bytes) store rows directly.
+        // O_t goes through tile t's Q buffer (free once O_t is final: every
+        // S_t product was issued before the last P_t V one) in the
+        // 128-byte-swizzled layout Q arrived in -- 16-byte chunk j of row r
+        // at j ^ (r % 8), so a warp's stores hit every bank once per
+        // wavefront -- and leaves in one TMA store per 64 head dims. The
+        // buffer holds all of a BF16 O tile; with E4M3 inputs (a Q tile of
+        // half the bytes) O goes in two passes of 64 head dims.
         const uint32_t obuf = sbase + C::kQOff + t * C::kQTileBytes;
+        constexpr uint32_t kOChunkBytes = BM * 128;                 // 64 BF16 head dims
+        constexpr int kOChunks = D / 64;
+        constexpr int kOPerPass = static_cast<int>(C::kQTileBytes / kOChunkBytes);
+        static_assert(kOPerPass >= 1 && kOChunks % kOPerPass == 0, "O passes");
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t ov[32];
@@ -589,30 +592,27 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int e = 0; e < 16; ++e)
                 pw[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l,
                                     __uint_as_float(ov[2 * e + 1]) * inv_l);
-            if constexpr (!F8) {
-                const uint32_t rbase = obuf + (cc / 2) * C::kQChunkBytes + r * 128;
+            const int oc = cc / 2;                                   // 64-dim chunk
+            const uint32_t rbase = obuf + (oc % kOPerPass) * kOChunkBytes + r * 128;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t j = (cc % 2) * 4 + e;
-                    ptx::st_shared_v4(rbase + ((j ^ (r & 7)) << 4), pw[4 * e], pw[4 * e + 1],
-                                      pw[4 * e + 2], pw[4 * e + 3]);
-                }
-            } else if (row < Nq) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t j = (cc % 2) * 4 + e;
+                ptx::st_shared_v4(rbase + ((j ^ (r & 7)) << 4), pw[4 * e], pw[4 * e + 1],
+                                  pw[4 * e + 2], pw[4 * e + 3]);
             }
-        }
-        if constexpr (!F8) {
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(1 + t, 4 * 32);                 // the tile's four warps
-            if (wq == 0 && lane == 0 && row_first < Nq) {
+            if (cc % 2 == 1 && (oc + 1) % kOPerPass == 0) {
+                // a pass is in shared memory: hand it to the TMA
+                ptx::fence_proxy_async_smem();
+                ptx::named_bar_sync(1 + t, 4 * 32);             // the tile's four warps
+                if (wq == 0 && lane == 0 && row_first < Nq) {
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    ptx::tma_store_3d(&tm_o, obuf + c * C::kQChunkBytes, c * 64, row_first, bh);
-                ptx::bulk_commit_group();
-                ptx::bulk_wait_read_all();       // the buffer outlives the copy's reads
+                    for (int c = oc + 1 - kOPerPass; c <= oc; ++c)
+                        ptx::tma_store_3d(&tm_o, obuf + (c % kOPerPass) * kOChunkBytes, c * 64,
+                                          row_first, bh);
+                    ptx::bulk_commit_group();
+                    ptx::bulk_wait_read_all();   // the buffer outlives the copy's reads
+                }
+                if (oc + 1 < kOChunks) ptx::named_bar_sync(1 + t, 4 * 32);   // buffer reusable
             }
         }
         if (lse != nullptr && row < Nq)
@@ -647,7 +647,7 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
     dim3 grid(pairs, a.H, a.B);
     const int reverse = (a.mask_kind & (kMaskCausal | kMaskWindow)) ? 1 : 0;
     fwd_sm103_kernel<D, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(
-        tq, tk, tv, to, static_cast<__nv_bfloat16*>(a.o), a.lse, a.H, a.Nq, a.Nk, scale_log2, o_mul,
+        tq, tk, tv, to, a.lse, a.H, a.Nq, a.Nk, scale_log2, o_mul,
         a.mask_kind, a.window, a.seqlens_k, a.err, reverse);
     return cudaGetLastError();
 }
