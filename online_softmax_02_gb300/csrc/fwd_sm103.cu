@@ -28,9 +28,12 @@
 //     block is read from device memory once per 256 queries, and the tensor
 //     core works on one tile's products while the other tile's softmax runs.
 //   * Warp 8 issues TMA bulk-tensor loads of Q (once) and streams K_j into a
-//     3-slot ring; warp 10 streams V_j into a 2-slot ring (5 and 5 at
-//     d = 64, 6 and 5 for E4M3); 128-byte-swizzled shared-memory buffers
-//     tracked by mbarriers with transaction counts.
+//     3-slot ring; warp 10 streams V_j into a 2-slot ring (5 and 4 at
+//     d = 64, 6 and 5 for E4M3); 128-byte-swizzled shared-memory buffers.
+//     K_j and V_{j-1}, the inputs of one MMA step, complete on one mbarrier
+//     with transaction counts, so the MMA warp waits once per step (each
+//     wait in its issue stream costs the tensor pipe: one wait fewer per
+//     block measured 1.415 -> 1.346 ms on the prefill).
 //   * Operand descriptors are built once per MMA group and advanced by the
 //     byte offset of each K-step (the issuing lane is on the critical path:
 //     this alone was worth 4 % of throughput).
@@ -116,9 +119,11 @@ struct Cfg {
     // K/V ring depths: K is consumed one MMA step ahead of V, so it gets the
     // deeper ring (BF16, d = 128: Q 64 KiB + K 3 x 32 KiB + V 2 x 32 KiB =
     // 224 KiB; E4M3: Q 32 KiB + K 6 x 16 KiB + V 5 x 16 KiB = 208 KiB, 1 %
-    // faster than 4 + 4 on the E4M3 prefill).
+    // faster than 4 + 4 on the E4M3 prefill). The V ring must be the
+    // shallower one: step barriers (one per K slot) also carry V.
     static constexpr int kStagesK = F8 ? 6 : (D == 64) ? 5 : 3;
-    static constexpr int kStagesV = F8 ? 5 : (D == 64) ? 5 : 2;
+    static constexpr int kStagesV = F8 ? 5 : (D == 64) ? 4 : 2;
+    static_assert(kStagesV < kStagesK, "a V load may not reach a step barrier's next phase");
     static constexpr uint32_t kRowBytes = 128;                 // one swizzle atom row
     static constexpr int kChunkElems = 128 / kElem;            // head dims per atom row
     static constexpr int kChunks = D * kElem / 128;
@@ -136,10 +141,9 @@ struct Cfg {
     static constexpr uint32_t kBarOff = kVOff + kStagesV * kKVBytes;
     // barrier indices
     static constexpr int bQFull = 0;
-    static constexpr int bKFull = 1;
-    static constexpr int bKEmpty = bKFull + kStagesK;
-    static constexpr int bVFull = bKEmpty + kStagesK;
-    static constexpr int bVEmpty = bVFull + kStagesV;
+    static constexpr int bStep = 1;                    // [NSK]: step s has K_s and V_{s-1}
+    static constexpr int bKEmpty = bStep + kStagesK;
+    static constexpr int bVEmpty = bKEmpty + kStagesK;
     static constexpr int bSFull = bVEmpty + kStagesV;
     static constexpr int bPFull = bSFull + NT;         // [NT]: P of the tile's block stored
     static constexpr int bODone = bPFull + NT;
@@ -236,13 +240,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == kProducerWarp && lane == 0) {
         ptx::mbar_init(bar(C::bQFull), 1);
         for (int s = 0; s < NSK; ++s) {
-            ptx::mbar_init(bar(C::bKFull + s), 1);
+            ptx::mbar_init(bar(C::bStep + s), 2);            // the K and the V producer
             ptx::mbar_init(bar(C::bKEmpty + s), 1);
         }
-        for (int s = 0; s < NSV; ++s) {
-            ptx::mbar_init(bar(C::bVFull + s), 1);
-            ptx::mbar_init(bar(C::bVEmpty + s), 1);
-        }
+        for (int s = 0; s < NSV; ++s) ptx::mbar_init(bar(C::bVEmpty + s), 1);
         for (int t = 0; t < NT; ++t) {
             ptx::mbar_init(bar(C::bSFull + t), 1);
             ptx::mbar_init(bar(C::bPFull + t), 4);           // one arrival per softmax warp
@@ -279,42 +280,66 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (warp == kProducerWarp || warp == kProducerVWarp) {
         // ------------------------------------------------------ TMA producers
         // Warp 8 (which started the Q loads above) streams K; warp 10
-        // streams V. Each ring is
-        // refilled as soon as a slot is released (by the softmax warp that
-        // sees the block's last S product complete). The whole warp runs the
-        // loop (uniform control flow); one elected lane issues.
+        // streams V. Each ring is refilled as soon as a slot is released (by
+        // the softmax warp that sees the block's last S product complete).
+        // Step i = s - lo of the MMA schedule reads K_s and V_{s-1}; both
+        // loads complete on step barrier i % NSK, which takes one arrival
+        // from each producer per phase (a plain one where the step has no
+        // such block: no V at the first step, no K at the last), so the MMA
+        // warp waits once per step. A producer arrives on step i's barrier
+        // only after the release of a block consumed at step i - NSK or
+        // later (K: K_{i-NSK}; V: V_{i-1-NSV}, with NSV < NSK), so the
+        // barrier's previous phase is always complete. The whole warp runs
+        // the loop (uniform control flow); one elected lane issues.
         if (lo < hi) {
             const bool leader = ptx::elect_one();
             const bool is_k = (warp == kProducerWarp);
             const int ns = is_k ? NSK : NSV;
-            const int full0 = is_k ? C::bKFull : C::bVFull;
             const int empty0 = is_k ? C::bKEmpty : C::bVEmpty;
             const uint32_t ring = sbase + (is_k ? C::kKOff : C::kVOff);
             const CUtensorMap* map = is_k ? &tm_k : &tm_v;
             if (leader) ptx::prefetch_tmap(map);
-            int issued = 0;
-            for (int s = lo; s < hi; ++s) {
-                const int i = s - lo, st = i % ns;
-                const uint32_t ph = (i / ns) & 1;
-                const bool got = wait_bounded(bar(empty0 + st), ph ^ 1, abort_flag, err,
-                                              is_k ? kSiteKEmpty : kSiteVEmpty);
-                if (!__all_sync(0xffffffffu, got)) break;
-                if (leader) {
-                    ptx::mbar_arrive_expect_tx(bar(full0 + st), C::kKVBytes);
-                    for (int c = 0; c < C::kChunks; ++c)
-                        ptx::tma_load_3d(ring + st * C::kKVBytes + c * C::kKVChunkBytes, map,
-                                         bar(full0 + st), c * C::kChunkElems, s * BN, bh);
+            const int n = hi - lo;
+            int issued = 0;                          // blocks whose copy has started
+            for (int i = 0; i <= n; ++i) {
+                const int b = is_k ? i : i - 1;      // block this producer adds to step i
+                const bool load = b >= 0 && b < n;
+                const uint32_t sb = bar(C::bStep + i % NSK);
+                if (load) {
+                    const int st = b % ns;
+                    const bool got = wait_bounded(bar(empty0 + st), ((b / ns) & 1) ^ 1, abort_flag,
+                                                  err, is_k ? kSiteKEmpty : kSiteVEmpty);
+                    if (!__all_sync(0xffffffffu, got)) break;
+                    if (leader) {
+                        ptx::mbar_arrive_expect_tx(sb, C::kKVBytes);
+                        for (int c = 0; c < C::kChunks; ++c)
+                            ptx::tma_load_3d(ring + st * C::kKVBytes + c * C::kKVChunkBytes, map, sb,
+                                             c * C::kChunkElems, (lo + b) * BN, bh);
+                    }
+                    issued = b + 1;
+                } else {
+                    // no block for this step: K at the last step; V at the
+                    // first. K's last-step arrival waits like a load would,
+                    // for the release of K_{n-NSK}.
+                    if (is_k && n >= NSK) {
+                        const bool got = wait_bounded(bar(empty0 + n % NSK), ((n / NSK) & 1) ^ 1,
+                                                      abort_flag, err, kSiteKEmpty);
+                        if (!__all_sync(0xffffffffu, got)) break;
+                    }
+                    if (leader) ptx::mbar_arrive(sb);
                 }
                 __syncwarp();
-                issued = i + 1;
             }
             if (*abort_flag && leader) {
-                // Let the copies this warp started land before the CTA exits.
+                // Let the copies this warp started land before the CTA exits
+                // (bounded: a step's phase also needs the other producer).
                 if (is_k)
                     wait_bounded(bar(C::bQFull), 0, nullptr, err, kSiteDrain, kWaitLimitCycles / 8);
-                for (int i = max(0, issued - ns); i < issued; ++i)
-                    wait_bounded(bar(full0 + i % ns), (i / ns) & 1, nullptr, err, kSiteDrain,
+                for (int b = max(0, issued - ns); b < issued; ++b) {
+                    const int i = is_k ? b : b + 1;
+                    wait_bounded(bar(C::bStep + i % NSK), (i / NSK) & 1, nullptr, err, kSiteDrain,
                                  kWaitLimitCycles / 8);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -335,22 +360,21 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                  wait_bounded(bar(C::bQFull), 0, abort_flag, err, kSiteQFull));
             for (int s = lo; ok && s <= hi; ++s) {
                 const int i = s - lo;
-                const int kst = i % NSK;                       // K slot of block s
+                const int kst = i % NSK;                       // K slot of block s = step barrier
                 const uint32_t kph = (i / NSK) & 1;
                 const int vst = (i + NSV - 1) % NSV;           // V slot of block s - 1
-                const uint32_t vph = ((i - 1) / NSV) & 1;
-                // Full barriers are waited right before their first use, and
-                // every block's barriers are waited once per step.
-                bool k_ready = !(s < hi), v_ready = !(s - 1 >= lo);
+                // The step barrier (K_s and V_{s-1} landed) is waited right
+                // before the step's first MMA, and once per step in any case.
+                bool kv_ready = false;
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (s - 1 >= R[t].lo && s - 1 < R[t].hi) {
                         // O_t (+)= P_t V_{s-1} once the softmax has stored P_t.
-                        if (!v_ready) {
-                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bVFull + vst), vph,
-                                                                      abort_flag, err, kSiteVFull));
+                        if (!kv_ready) {
+                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), kph,
+                                                                      abort_flag, err, kSiteKFull));
                             if (!ok) break;
-                            v_ready = true;
+                            kv_ready = true;
                         }
                         const uint32_t vbase = sbase + C::kVOff + vst * C::kKVBytes;
                         const uint64_t vdesc0 = ptx::sdesc_sw128(vbase, C::kKVChunkBytes, 1024);
@@ -380,12 +404,12 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     if (s < hi && s >= R[t].lo && s < R[t].hi) {
                         // S_t = Q_t K_s^T
-                        if (!k_ready) {
-                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKFull + kst), kph,
+                        if (!kv_ready) {
+                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), kph,
                                                                       abort_flag, err, kSiteKFull));
                             if (!ok) break;
                             ptx::tc_fence_after();
-                            k_ready = true;
+                            kv_ready = true;
                         }
                         const uint32_t qbase = sbase + C::kQOff + t * C::kQTileBytes;
                         const uint32_t kbase = sbase + C::kKOff + kst * C::kKVBytes;
@@ -411,11 +435,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
                 if (!ok) break;
-                if (!v_ready)
-                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bVFull + vst), vph, abort_flag,
-                                                              err, kSiteVFull));
-                if (ok && !k_ready)
-                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bKFull + kst), kph, abort_flag,
+                if (!kv_ready)
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), kph, abort_flag,
                                                               err, kSiteKFull));
                 if (!ok) break;
                 // K_s and V_{s-1} are released by the softmax (no commit here:
