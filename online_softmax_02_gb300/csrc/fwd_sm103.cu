@@ -56,8 +56,8 @@
 //     the epilogue O = A / l and lse, O leaving (BF16 inputs) through the
 //     tile's dead Q buffer and a TMA store.
 //   * m, l and A are FP32; P is rounded to BF16 for the P V product.
-//   * Exponentials: ex2.approx on the MUFU unit, except (BF16) one pair in
-//     every 16, which runs as a polynomial on the FMA pipe (soft_exp2x2:
+//   * Exponentials: ex2.approx on the MUFU unit; a compile-time fraction of
+//     them can run as a polynomial on the FMA pipe instead (soft_exp2x2:
 //     relative error 1.02e-4, below P's BF16 rounding).
 //   * E4M3 variant (d = 128): Q, K and V are 8-bit floats with per-tensor
 //     dequantisation factors, the FP8 mode that P1 ("What did
@@ -93,12 +93,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;
 // Of every 16 pairs of exponentials of P, this many are computed in software
 // on the FMA pipe (soft_exp2x2) and the rest by ex2.approx on the MUFU unit,
-// spread evenly through the group. Measured on GB300 (prefill B1 H64 8192^2
-// d128): BF16 1390 / 1408 / 1354 / 1313 / 1241 TFLOP/s with 0 / 1 / 2 / 4 /
-// 8 pairs, E4M3 1756 / 1667 / 1622 / 1501 / 1352: the softmax phase is bound
-// by latency and issue slots, not by the MUFU unit's throughput.
+// spread evenly through the group (a compile-time choice). With the MMA
+// issue stream slimmed down the softmax has slack and every extra
+// instruction in it shows: prefill B1 H64 8192^2 d128 1.312 / 1.319 /
+// 1.378 ms with 0 / 1 / 2 pairs (BF16), causal 0.731 / 0.744 / 0.763 ms,
+// E4M3 1.064 / 1.110 ms with 0 / 1. (An earlier build, whose softmax was
+// on the critical path, measured 1 pair fastest for BF16.)
 #ifndef ATTN_SOFT_EXP2_PAIRS_BF16
-#define ATTN_SOFT_EXP2_PAIRS_BF16 1
+#define ATTN_SOFT_EXP2_PAIRS_BF16 0
 #endif
 #ifndef ATTN_SOFT_EXP2_PAIRS_E4M3
 #define ATTN_SOFT_EXP2_PAIRS_E4M3 0
