@@ -601,46 +601,48 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         constexpr int kOChunks = D / 64;
         constexpr int kOPerPass = static_cast<int>(C::kQTileBytes / kOChunkBytes);
         static_assert(kOPerPass >= 1 && kOChunks % kOPerPass == 0, "O passes");
+        const bool issuer = wq == 0 && lane == 0 && row_first < Nq;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t ov[32];
+        for (int oc = 0; oc < kOChunks; ++oc) {                     // 64 head dims at a time
+            uint32_t ov[64];
             if (have) {
-                ptx::tmem_ld32x32b_x32(o_addr + cc * 32, ov);
+                ptx::tmem_ld32x32b_x64(o_addr + oc * 64, ov);
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) ov[e] = 0u;
+                for (int e = 0; e < 64; ++e) ov[e] = 0u;
             }
-            uint32_t pw[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                pw[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l,
-                                    __uint_as_float(ov[2 * e + 1]) * inv_l);
-            const int oc = cc / 2;                                   // 64-dim chunk
             const uint32_t rbase = obuf + (oc % kOPerPass) * kOChunkBytes + r * 128;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t j = (cc % 2) * 4 + e;
-                ptx::st_shared_v4(rbase + ((j ^ (r & 7)) << 4), pw[4 * e], pw[4 * e + 1],
-                                  pw[4 * e + 2], pw[4 * e + 3]);
+            for (int jc = 0; jc < 8; ++jc) {                           // 16-byte chunks of the row
+                uint32_t pw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    pw[e] = pack_bf16x2(__uint_as_float(ov[8 * jc + 2 * e]) * inv_l,
+                                        __uint_as_float(ov[8 * jc + 2 * e + 1]) * inv_l);
+                ptx::st_shared_v4(rbase + ((jc ^ (r & 7)) << 4), pw[0], pw[1], pw[2], pw[3]);
             }
-            if (cc % 2 == 1 && (oc + 1) % kOPerPass == 0) {
+            if ((oc + 1) % kOPerPass == 0) {
                 // a pass is in shared memory: hand it to the TMA
                 ptx::fence_proxy_async_smem();
                 ptx::named_bar_sync(1 + t, 4 * 32);             // the tile's four warps
-                if (wq == 0 && lane == 0 && row_first < Nq) {
+                if (issuer) {
 #pragma unroll
                     for (int c = oc + 1 - kOPerPass; c <= oc; ++c)
                         ptx::tma_store_3d(&tm_o, obuf + (c % kOPerPass) * kOChunkBytes, c * 64,
                                           row_first, bh);
                     ptx::bulk_commit_group();
-                    ptx::bulk_wait_read_all();   // the buffer outlives the copy's reads
                 }
-                if (oc + 1 < kOChunks) ptx::named_bar_sync(1 + t, 4 * 32);   // buffer reusable
+                if (oc + 1 < kOChunks) {
+                    // the buffer is reused by the next pass once the copy has read it
+                    if (issuer) ptx::bulk_wait_read_all();
+                    ptx::named_bar_sync(1 + t, 4 * 32);
+                }
             }
         }
         if (lse != nullptr && row < Nq)
             lse[static_cast<long long>(bh) * Nq + row] =
                 (l > 0.f) ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+        if (issuer) ptx::bulk_wait_read_all();   // the buffer outlives the copy's reads
     }
 
     ptx::tc_fence_before();

@@ -312,3 +312,24 @@ def test_fwd_from_host_matches_device_call(cuda_lib, orc, shape):
     assert np.array_equal(hl.numpy(), l_dev)
     ro, rl = oracle_fwd(orc, x, mk, win)
     assert_close(ho.float().numpy(), hl.numpy(), ro, rl, TOL_O_BF16, TOL_LSE, what=str(shape))
+
+
+@pytest.mark.parametrize("chunks,slots", [(5, 2), (7, 4), (3, 1)])
+def test_fwd_from_host_slot_counts(cuda_lib, chunks, slots):
+    """The host pipeline with fewer or more device slots than the default
+    (each slot reused once its previous group has been copied out) gives
+    the device-resident result bit for bit."""
+    B, H, Nq, Nk, d = 2, 4, 300, 420, 128
+    x = W.random_inputs(B, H, Nq, Nk, d, seed=77 + slots)
+    o_dev, l_dev = run_fwd(cuda_lib, x, W.MASK_CAUSAL)
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.zeros(B, H, Nq, d, dtype=torch.bfloat16).pin_memory()
+    hl = torch.zeros(B, H, Nq, dtype=torch.float32).pin_memory()
+    pipe = cuda_lib.HostPipeline(B, H, Nq, Nk, d, chunks=chunks, slots=slots)
+    for _ in range(2):                       # the pipeline is reusable across calls
+        ho.zero_()
+        cuda_lib.attn_fwd_from_host(hq, hk, hv, ho, hl, mask_kind=W.MASK_CAUSAL, pipeline=pipe)
+        torch.cuda.synchronize()
+        cuda_lib.attn_check_device_error()
+        assert np.array_equal(ho.float().numpy(), o_dev)
+        assert np.array_equal(hl.numpy(), l_dev)
