@@ -299,75 +299,83 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // buffer u % kBufs. Issue order S(0), S(1), G(0), S(2), G(1), ...:
             // the products of unit u run while the row warps work on unit
             // u - 1, and G(u - 1) (dV, dK) follows as soon as they are done.
-            const int nu = 2 * nblk;
-            constexpr int L = C::kBufs - 1;      // G(v) is issued after S(v + L)
-            for (int u = 0; ok && u < nu + L; ++u) {
-                if (u < nu) {
-                    const int i = u / 2, hh = u % 2, st = i % NSB, bf = u % C::kBufs;
-                    if (hh == 0) {
-                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bInFull + st), (i / NSB) & 1,
-                                                                  abort_flag, err, kSiteKFull));
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                    }
-                    if (leader) {
-                        // S^T = K Q_hh^T and dP^T = V dO_hh^T (M = 128 keys, N = 64 queries)
-                        const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
-                        const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
-                        const uint64_t kd0 = ptx::sdesc_sw128(sbase + C::kKOff, 16, 1024);
-                        const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::kVOff, 16, 1024);
-                        const uint64_t qd0 = ptx::sdesc_sw128(qh, 16, 1024);
-                        const uint64_t dd0 = ptx::sdesc_sw128(dh, 16, 1024);
+            static_assert(C::kBufs == 2, "G(u - 1) follows S(u); buffer = query half");
+            auto do_s = [&](int i, int hh) {         // S^T, dP^T of unit 2 i + hh
+                const int st = i % NSB, bf = hh;
+                if (leader) {
+                    // S^T = K Q_hh^T and dP^T = V dO_hh^T (M = 128 keys, N = 64 queries)
+                    const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
+                    const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
+                    const uint64_t kd0 = ptx::sdesc_sw128(sbase + C::kKOff, 16, 1024);
+                    const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::kVOff, 16, 1024);
+                    const uint64_t qd0 = ptx::sdesc_sw128(qh, 16, 1024);
+                    const uint64_t dd0 = ptx::sdesc_sw128(dh, 16, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_add(kd0, off), ptx::sdesc_add(qd0, off),
-                                        kIdS, kk > 0 ? 1u : 0u);
-                        }
-                        ptx::mma_commit(bar(C::bS + bf));
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_add(vd0, off), ptx::sdesc_add(dd0, off),
-                                        kIdS, kk > 0 ? 1u : 0u);
-                        }
-                        ptx::mma_commit(bar(C::bDP + bf));
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                        ptx::mma_ss(tmem + C::cS(bf), ptx::sdesc_add(kd0, off),
+                                    ptx::sdesc_add(qd0, off), kIdS, kk > 0 ? 1u : 0u);
                     }
-                    __syncwarp();
+                    ptx::mma_commit(bar(C::bS + bf));
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+                        ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_add(vd0, off),
+                                    ptx::sdesc_add(dd0, off), kIdS, kk > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(bar(C::bDP + bf));
                 }
-                if (u >= L) {
-                    const int v = u - L, i = v / 2, hh = v % 2, st = i % NSB, bf = v % C::kBufs;
-                    const uint32_t vph = (v / C::kBufs) & 1;
-                    // one wait for both products: dS^T stored implies P^T stored
-                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bDS + bf), vph, abort_flag, err,
-                                                              kSitePFull));
-                    if (!ok) break;
-                    ptx::tc_fence_after();
+                __syncwarp();
+            };
+            auto do_g = [&](int i, int hh) {         // dV, dK of unit v = 2 i + hh
+                const int v = 2 * i + hh, st = i % NSB, bf = hh;
+                // one wait for both products: dS^T stored implies P^T stored
+                const bool got = __all_sync(0xffffffffu,
+                                            wait_bounded(bar(C::bDS + bf), (v / C::kBufs) & 1,
+                                                         abort_flag, err, kSitePFull));
+                if (!got) return false;
+                ptx::tc_fence_after();
+                if (leader) {
                     const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
                     const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
                     const uint64_t qg0 = ptx::sdesc_sw128(qh, C::kChunkBytes, 1024);
                     const uint64_t dg0 = ptx::sdesc_sw128(dh, C::kChunkBytes, 1024);
-                    if (leader) {
-                        // dV += P^T dO_hh (A from TMEM, B MN-major, K = 64 queries)
+                    // dV += P^T dO_hh (A from TMEM, B MN-major, K = 64 queries)
 #pragma unroll
-                        for (int kk = 0; kk < BU / 16; ++kk)
-                            ptx::mma_ts(tmem + C::cDV, tmem + C::cS(bf) + a_col(kk),
-                                        ptx::sdesc_add(dg0, kk * 16 * C::kRowBytes),
-                                        kIdG, (v > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    __syncwarp();
-                    if (leader) {
-                        // dK += dS^T Q_hh
+                    for (int kk = 0; kk < BU / 16; ++kk)
+                        ptx::mma_ts(tmem + C::cDV, tmem + C::cS(bf) + a_col(kk),
+                                    ptx::sdesc_add(dg0, kk * 16 * C::kRowBytes), kIdG,
+                                    (v > 0 || kk > 0) ? 1u : 0u);
+                    // dK += dS^T Q_hh
 #pragma unroll
-                        for (int kk = 0; kk < BU / 16; ++kk)
-                            ptx::mma_ts(tmem + C::cDK, tmem + C::cDP(bf) + a_col(kk),
-                                        ptx::sdesc_add(qg0, kk * 16 * C::kRowBytes),
-                                        kIdG, (v > 0 || kk > 0) ? 1u : 0u);
-                        if (hh == 1) ptx::mma_commit(bar(C::bInEmpty + st));
-                    }
-                    __syncwarp();
+                    for (int kk = 0; kk < BU / 16; ++kk)
+                        ptx::mma_ts(tmem + C::cDK, tmem + C::cDP(bf) + a_col(kk),
+                                    ptx::sdesc_add(qg0, kk * 16 * C::kRowBytes), kIdG,
+                                    (v > 0 || kk > 0) ? 1u : 0u);
+                    // after the block's second unit, its Q/dO stage is free
+                    if (hh == 1) ptx::mma_commit(bar(C::bInEmpty + st));
                 }
+                __syncwarp();
+                return true;
+            };
+            auto wait_in = [&](int i) {              // Q/dO of block i landed
+                const bool got = __all_sync(0xffffffffu,
+                                            wait_bounded(bar(C::bInFull + i % NSB), (i / NSB) & 1,
+                                                         abort_flag, err, kSiteKFull));
+                if (got) ptx::tc_fence_after();
+                return got;
+            };
+            // Block by block: S(2i), G(2i - 1), S(2i + 1), G(2i); the loop
+            // body has no tests beyond the waits' own.
+            if (ok && (ok = wait_in(0))) { do_s(0, 0); do_s(0, 1); ok = do_g(0, 0); }
+            for (int i = 1; ok && i < nblk; ++i) {
+                if (!(ok = wait_in(i))) break;
+                do_s(i, 0);
+                if (!(ok = do_g(i - 1, 1))) break;
+                do_s(i, 1);
+                ok = do_g(i, 0);
             }
+            if (ok) ok = do_g(nblk - 1, 1);
             if (leader) ptx::mma_commit(bar(C::bDone));
             __syncwarp();
             wait_bounded(bar(C::bDone), 0, nullptr, err, kSiteDrain);
@@ -614,56 +622,62 @@ bwd_dq_kernel(const __nv_bfloat16* __restrict__ qg, const __grid_constant__ CUte
             // G(1), ...: the products run one unit ahead of the row warps;
             // the row warps release a unit's K/V slot (below).
             const int nu = 2 * nblk;
-            constexpr int L = C::kBufs - 1;      // G(v) is issued after S(v + L)
-            for (int u = 0; ok && u < nu + L; ++u) {
-                if (u < nu) {
-                    const int st = u % C::NSU, bf = u % C::kBufs;
-                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bUFull + st), (u / C::NSU) & 1,
-                                                              abort_flag, err, kSiteKFull));
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    if (leader) {
-                        // S = Q K_u^T, dP = dO V_u^T (M = 128 queries, N = 64 keys);
-                        // A = Q or dO from tensor memory (8 columns per 16 head
-                        // dims), B = the K or V unit from shared memory
-                        const uint64_t kd0 = ptx::sdesc_sw128(sbase + C::k_off(st), 16, 1024);
-                        const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::v_off(st), 16, 1024);
+            static_assert(C::kBufs == 2, "G(u - 1) follows S(u)");
+            auto do_s = [&](int u) {                 // wait for K/V unit u; S(u), dP(u)
+                const int st = u % C::NSU, bf = u % C::kBufs;
+                const bool got = __all_sync(0xffffffffu,
+                                            wait_bounded(bar(C::bUFull + st), (u / C::NSU) & 1,
+                                                         abort_flag, err, kSiteKFull));
+                if (!got) return false;
+                ptx::tc_fence_after();
+                if (leader) {
+                    // S = Q K_u^T, dP = dO V_u^T (M = 128 queries, N = 64 keys);
+                    // A = Q or dO from tensor memory (8 columns per 16 head
+                    // dims), B = the K or V unit from shared memory
+                    const uint64_t kd0 = ptx::sdesc_sw128(sbase + C::k_off(st), 16, 1024);
+                    const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::v_off(st), 16, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t boff = (kk / 4) * C::kUChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ts(tmem + C::cS(bf), tmem + C::cQ + kk * 8,
-                                        ptx::sdesc_add(kd0, boff), kIdS, kk > 0 ? 1u : 0u);
-                        }
-                        ptx::mma_commit(bar(C::bS + bf));
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t boff = (kk / 4) * C::kUChunkBytes + (kk % 4) * 32;
-                            ptx::mma_ts(tmem + C::cDP(bf), tmem + C::cDO + kk * 8,
-                                        ptx::sdesc_add(vd0, boff), kIdS, kk > 0 ? 1u : 0u);
-                        }
-                        ptx::mma_commit(bar(C::bDP + bf));
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t boff = (kk / 4) * C::kUChunkBytes + (kk % 4) * 32;
+                        ptx::mma_ts(tmem + C::cS(bf), tmem + C::cQ + kk * 8,
+                                    ptx::sdesc_add(kd0, boff), kIdS, kk > 0 ? 1u : 0u);
                     }
-                    __syncwarp();
-                }
-                if (u >= L) {
-                    const int v = u - L, st = v % C::NSU, bf = v % C::kBufs;
-                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bP + bf), (v / C::kBufs) & 1, abort_flag,
-                                                              err, kSitePFull));
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    if (leader) {
-                        // dQ += dS K_u (A = dS from TMEM, B = K MN-major, K = 64 keys)
-                        const uint64_t kg0 =
-                            ptx::sdesc_sw128(sbase + C::k_off(st), C::kUChunkBytes, 1024);
+                    ptx::mma_commit(bar(C::bS + bf));
 #pragma unroll
-                        for (int kk = 0; kk < BU / 16; ++kk)
-                            ptx::mma_ts(tmem + C::cDQ, tmem + C::cS(bf) + a_col(kk),
-                                        ptx::sdesc_add(kg0, kk * 16 * C::kRowBytes),
-                                        kIdG, (v > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t boff = (kk / 4) * C::kUChunkBytes + (kk % 4) * 32;
+                        ptx::mma_ts(tmem + C::cDP(bf), tmem + C::cDO + kk * 8,
+                                    ptx::sdesc_add(vd0, boff), kIdS, kk > 0 ? 1u : 0u);
                     }
-                    __syncwarp();
+                    ptx::mma_commit(bar(C::bDP + bf));
                 }
-            }
+                __syncwarp();
+                return true;
+            };
+            auto do_g = [&](int v) {                 // wait for dS(v); dQ += dS K_v
+                const int st = v % C::NSU, bf = v % C::kBufs;
+                const bool got = __all_sync(0xffffffffu,
+                                            wait_bounded(bar(C::bP + bf), (v / C::kBufs) & 1,
+                                                         abort_flag, err, kSitePFull));
+                if (!got) return false;
+                ptx::tc_fence_after();
+                if (leader) {
+                    // dQ += dS K_u (A = dS from TMEM, B = K MN-major, K = 64 keys)
+                    const uint64_t kg0 = ptx::sdesc_sw128(sbase + C::k_off(st), C::kUChunkBytes, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BU / 16; ++kk)
+                        ptx::mma_ts(tmem + C::cDQ, tmem + C::cS(bf) + a_col(kk),
+                                    ptx::sdesc_add(kg0, kk * 16 * C::kRowBytes), kIdG,
+                                    (v > 0 || kk > 0) ? 1u : 0u);
+                }
+                __syncwarp();
+                return true;
+            };
+            // S(0), then S(u), G(u - 1) for u = 1 .. nu - 1, then G(nu - 1):
+            // the loop body has no tests beyond the waits' own.
+            if (nu > 0) ok = ok && do_s(0);
+            for (int u = 1; ok && u < nu; ++u) ok = do_s(u) && do_g(u - 1);
+            if (ok && nu > 0) ok = do_g(nu - 1);
             if (leader) ptx::mma_commit(bar(C::bDone));
             __syncwarp();
             wait_bounded(bar(C::bDone), 0, nullptr, err, kSiteDrain);
