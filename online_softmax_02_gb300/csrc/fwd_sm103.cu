@@ -399,10 +399,14 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // prefill 1.315 -> 1.289 ms). The E4M3 kernel, whose softmax is
             // the longer chain, measured 1.063 -> 1.098 ms with it and keeps
             // the general loop.
-            const bool uniform = !F8 && R[0].lo == lo && R[1].lo == lo && R[0].hi == hi &&
-                                 R[1].hi == hi;
+            // A causal tile 1 covers one block more than tile 0 (the
+            // diagonal block of its own rows): the same loop up to tile 0's
+            // last step, then one step of tile 1's.
+            const int h0 = R[0].hi, h1 = R[1].hi;
+            const bool uniform = !F8 && R[0].lo == lo && R[1].lo == lo && h1 == hi &&
+                                 (h0 == hi || h0 == hi - 1);
             if (ok && uniform) {
-                for (int s = lo; s <= hi; ++s) {
+                for (int s = lo; s <= h0; ++s) {
                     const int i = s - lo;
                     const int kst = i % NSK;
                     const int vst = (i + NSV - 1) % NSV;
@@ -419,16 +423,33 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             ptx::tc_fence_after();
                             if (leader) {
                                 issue_pv(t, vst, i == 1);
-                                if (s == hi) ptx::mma_commit(bar(C::bODone + t));
+                                if (s == R[t].hi) ptx::mma_commit(bar(C::bODone + t));
                             }
                             __syncwarp();
                         }
-                        if (s < hi) {
+                        if (s < R[t].hi) {
                             if (leader) issue_s(t, kst);
                             __syncwarp();
                         }
                     }
                     if (!ok) break;
+                }
+                if (ok && h0 < hi) {
+                    // tile 1's last P V product (step hi)
+                    const int i = hi - lo;
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + i % NSK), (i / NSK) & 1,
+                                                              abort_flag, err, kSiteKFull));
+                    if (ok)
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + 1), (i - 1) & 1,
+                                                                  abort_flag, err, kSitePFull));
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        if (leader) {
+                            issue_pv(1, (i + NSV - 1) % NSV, i == 1);
+                            ptx::mma_commit(bar(C::bODone + 1));
+                        }
+                        __syncwarp();
+                    }
                 }
             }
             for (int s = lo; ok && !uniform && s <= hi; ++s) {
