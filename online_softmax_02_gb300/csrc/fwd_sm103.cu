@@ -27,7 +27,8 @@
 //   * Two query tiles per CTA (256 rows) share every K/V block, so each
 //     block is read from device memory once per 256 queries, and the tensor
 //     core works on one tile's products while the other tile's softmax runs.
-//   * Warp 8 issues TMA bulk-tensor loads of Q (once) and streams K_j into a
+//   * Warp 8 issues TMA bulk-tensor loads of Q (once, before the CTA's
+//     set-up, which they overlap) and streams K_j into a
 //     3-slot ring; warp 10 streams V_j into a 2-slot ring (5 and 4 at
 //     d = 64, 6 and 5 for E4M3); 128-byte-swizzled shared-memory buffers.
 //     K_j and V_{j-1}, the inputs of one MMA step, complete on one mbarrier
@@ -43,7 +44,12 @@
 //     lane elected with elect.sync issues every tcgen05.mma: S_t = Q_t K_j^T with both
 //     operands in shared memory, and O_t += P_t V_j with P_t read from tensor
 //     memory (BF16, written over S_t) and V_j from shared memory. Issue order
-//     per block: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j).
+//     per block: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). The MMA warp commits
+//     only S and the final O; the K and V slots are released by the softmax
+//     warp that sees the block's last S product complete. BF16 CTAs whose
+//     tiles cover the same blocks (and causal ones, up to tile 0's last
+//     block) run a straight-line version of the schedule without per-tile
+//     range tests.
 //   * Warps 0-3 run the softmax of tile 0 and warps 4-7 that of tile 1, one
 //     thread per query row: tcgen05.ld of the 128 scores of its row, mask,
 //     row max (four independent three-input max chains) and row sum (packed
@@ -53,8 +59,8 @@
 //     warp reaches a tile's P V product well after its P is ready, so a
 //     separate hand-off per half only adds a wait to the issue stream: one
 //     hand-off per tile measured 1.507 -> 1.439 ms on the prefill); then
-//     the epilogue O = A / l and lse, O leaving (BF16 inputs) through the
-//     tile's dead Q buffer and a TMA store.
+//     the epilogue O = A / l and lse, O leaving through the tile's dead Q
+//     buffer and TMA stores (E4M3: in two passes of 64 head dims).
 //   * m, l and A are FP32; P is rounded to BF16 for the P V product.
 //   * Exponentials: ex2.approx on the MUFU unit; a compile-time fraction of
 //     them can run as a polynomial on the FMA pipe instead (soft_exp2x2:
