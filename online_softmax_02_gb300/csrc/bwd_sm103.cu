@@ -29,13 +29,17 @@
 // (4 x 64 columns) and its dK and dV accumulators (2 x 128 at d = 128), and
 // no dQ tile beside them.
 //
-// Pipelining. The unit buffers (two in the dK/dV kernel; three in the dQ
-// kernel, whose K and V arrive as 64-key units in a ring of four slots) let
-// the MMA warp issue the next units' products while the row warps work; S and dP are committed separately, so
-// the row warps compute P as soon as S is done (while dP's product runs);
-// in the dK/dV kernel dV's and dK's products are issued together once dS^T
-// is stored (one wait in the issue stream instead of two: 5.66 -> 5.60 ms). Row work goes 32 columns at a time with the block's LSE
-// and D read as 16-byte shared-memory vectors.
+// Pipelining. Two unit buffers in tensor memory per kernel (in the dQ
+// kernel K and V arrive as 64-key units in a ring of six slots, which the
+// row warps release; Q and dO sit in tensor memory as the A operand of the
+// score products) let the MMA warp issue the next unit's products while
+// the row warps work; S and dP are committed separately, so the row warps
+// compute P as soon as S is done (while dP's product runs); in the dK/dV
+// kernel dV's and dK's products are issued together once dS^T is stored
+// (one wait in the issue stream instead of two: 5.66 -> 5.60 ms). Row work
+// goes 32 columns at a time with the block's LSE and D read as 16-byte
+// shared-memory vectors. Both MMA loops are peeled so that their bodies
+// hold no tests beyond the waits.
 // Measured on GB300 (B1 H64 8192^2 d128): with the element-wise work taken
 // out the two kernels are only 8 % faster, so the limit is the MMA issue
 // stream itself (waits between the single issuer's groups drain the short
