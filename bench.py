@@ -54,11 +54,11 @@ NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
     # launch at the full bench workload, 1-pass ncu capture (profiles/
     # ncu_traffic_full_size.md); valid while the kernel source is unchanged.
-    "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": "2694096d34aeaf4c94610b52619a27d175f6479ecf4ed93d09cdfbefb29e0123",
-                 "bytes_per_launch": 402971136 + 115525120,
+    "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": "195b3626a3f55a77002b8c722fe2ec8e77fecb64aa32e0ae5d772e323a6faa6b",
+                 "bytes_per_launch": 402933504 + 115678464,
                  "workload": "prefill_B1_H64_N8192_d128_bf16"},
-    "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": "2694096d34aeaf4c94610b52619a27d175f6479ecf4ed93d09cdfbefb29e0123",
-                 "bytes_per_launch": 201552640 + 102795520,
+    "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": "195b3626a3f55a77002b8c722fe2ec8e77fecb64aa32e0ae5d772e323a6faa6b",
+                 "bytes_per_launch": 201414144 + 104146432,
                  "workload": "prefill_B1_H64_N8192_d128_e4m3"},
     "decode": {"file": "decode.cu",
                "sha256": "1307a0be67d90977d4847a9f6c760c5b2d48dad081c5b803233a750d89e4f405",
