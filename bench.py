@@ -18,8 +18,9 @@ workload on its own GPU (no collective on the data path: the problems are
 independent); a barrier and a max over ranks bracket the timed region and
 `value` counts the work of all ranks ("scaling": "weak").
 
---impl reference times the FP64 CPU oracle (the reference implementation of
-this build) on a bounded sample of the same workload, on the host cores.
+--impl reference times the FP64 CPU oracle (the reference implementation
+the GPU results are checked against) on a bounded sample of the same
+workload, on the host cores.
 """
 from __future__ import annotations
 
