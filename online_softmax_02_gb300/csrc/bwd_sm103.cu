@@ -154,35 +154,49 @@ __device__ __forceinline__ bool visible(int q, int key, int Lk, bool causal, boo
 }
 
 // ---------------------------------------------------------------- prep
-// One warp per query row: D = <dO_i, O_i>, LSE2 = LSE * log2(e).
+// D = <dO_i, O_i> and LSE * log2(e) per query row. D / 8 lanes share a row,
+// each reading 16 bytes of O and of dO (a warp covers 32 * 16 B of each per
+// load: the kernel is a stream over O and dO), reduced by shuffles within
+// the row's lanes.
 template <int D>
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                 const float* __restrict__ lse, float* __restrict__ ws_lse2,
                 float* __restrict__ ws_dd, int Nq, int Nq_pad, long long rows_pad) {
-    const long long wrow = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32;
-    const int lane = threadIdx.x % 32;
-    if (wrow >= rows_pad) return;
-    const long long bh = wrow / Nq_pad;
-    const int i = static_cast<int>(wrow % Nq_pad);
-    if (i >= Nq) {
-        if (lane == 0) { ws_lse2[wrow] = INFINITY; ws_dd[wrow] = 0.f; }
-        return;
-    }
-    const long long src = (bh * Nq + i) * D;
+    constexpr int kLanesPerRow = D / 8;
+    static_assert(32 % kLanesPerRow == 0, "rows must not straddle warps");
+    const long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    const long long wrow = t / kLanesPerRow;
+    const int sub = static_cast<int>(t % kLanesPerRow);
+    const bool in = wrow < rows_pad;
+    const long long bh = in ? wrow / Nq_pad : 0;
+    const int i = in ? static_cast<int>(wrow % Nq_pad) : 0;
+    const bool real = in && i < Nq;
     float acc = 0.f;
-    for (int e = lane * 2; e < D; e += 64) {
-        const uint32_t ow = *reinterpret_cast<const uint32_t*>(o + src + e);
-        const uint32_t dw = *reinterpret_cast<const uint32_t*>(dout + src + e);
-        acc = fmaf(bf16lo_to_f32(ow), bf16lo_to_f32(dw), acc);
-        acc = fmaf(bf16hi_to_f32(ow), bf16hi_to_f32(dw), acc);
+    if (real) {
+        const long long src = (bh * Nq + i) * D + sub * 8;
+        const uint4 ow = *reinterpret_cast<const uint4*>(o + src);
+        const uint4 dw = *reinterpret_cast<const uint4*>(dout + src);
+        const uint32_t ov[4] = {ow.x, ow.y, ow.z, ow.w}, dv[4] = {dw.x, dw.y, dw.z, dw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(bf16lo_to_f32(ov[e]), bf16lo_to_f32(dv[e]), acc);
+            acc = fmaf(bf16hi_to_f32(ov[e]), bf16hi_to_f32(dv[e]), acc);
+        }
     }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        const float l = lse[bh * Nq + i];
-        ws_lse2[wrow] = (l == -INFINITY) ? -INFINITY : l * kLog2eB;
-        ws_dd[wrow] = acc;
+    for (int off = kLanesPerRow / 2; off >= 1; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (in && sub == 0) {
+        if (real) {
+            const float l = lse[bh * Nq + i];
+            ws_lse2[wrow] = (l == -INFINITY) ? -INFINITY : l * kLog2eB;
+            ws_dd[wrow] = acc;
+        } else {
+            // padding rows: lse = +inf, D = 0, so they contribute P = 0
+            ws_lse2[wrow] = INFINITY;
+            ws_dd[wrow] = 0.f;
+        }
     }
 }
 
@@ -854,9 +868,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     const int Nq_pad = (a.Nq + BT - 1) / BT * BT;
     const long long rows_pad = static_cast<long long>(a.B) * a.H * Nq_pad;
     const float scale_log2 = a.scale * kLog2eB;
-    const int warps_per_block = 256 / 32;
-    bwd_prep_kernel<D><<<static_cast<unsigned>((rows_pad + warps_per_block - 1) / warps_per_block),
-                         256, 0, stream>>>(
+    const long long prep_threads = rows_pad * (D / 8);
+    bwd_prep_kernel<D><<<static_cast<unsigned>((prep_threads + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
         a.ws_lse2, a.ws_dd, a.Nq, Nq_pad, rows_pad);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
