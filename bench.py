@@ -62,8 +62,8 @@ NCU_TRAFFIC = {
                  "bytes_per_launch": 201414144 + 104146432,
                  "workload": "prefill_B1_H64_N8192_d128_e4m3"},
     "decode": {"file": "decode.cu",
-               "sha256": "1307a0be67d90977d4847a9f6c760c5b2d48dad081c5b803233a750d89e4f405",
-               "bytes_per_launch": 2147748864 + 3136768,
+               "sha256": "1e8433d0c2c945f4dff3e0d753f60c24f853a2730e97cfd0e826e9ce628a67d1",
+               "bytes_per_launch": 2147533056 + 3133184,
                "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split kernel)"},
     "softmax": {"file": "softmax.cu",
                 "sha256": "9a40d74a21d385c58919240ac5c54e555e31ccc3e2bd568868bc0f51f562068d",

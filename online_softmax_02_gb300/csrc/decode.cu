@@ -14,6 +14,10 @@
 // Launch 2, decode_combine_kernel: grid (H, B). Merges the chunks of one
 // (b, h) with the associative rule of P3 "Step 4": m* = max_s lse_s,
 // w_s = exp(lse_s - m*), o = sum w_s o_s / sum w_s, lse = m* + log sum w_s.
+// It is a programmatic dependent launch: its CTAs may be scheduled while
+// the split kernel's last wave runs, and wait (griddepcontrol.wait) for
+// that grid's completion and memory before reading any partial, which
+// hides most of the gap between the two launches.
 //
 // The work is one multiply-add per key element for the scores and one for
 // the output: the split kernel is bound by HBM bandwidth. Each warp streams
@@ -73,6 +77,8 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     constexpr int LPK = D / 8;        // lanes per key row (16 bytes each)
     constexpr int KPI = 32 / LPK;     // keys per warp load instruction
     constexpr int KPB = KPI * kUnroll;  // keys per batch per warp
+    // the combine launch may start now; it waits for this grid to complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     __shared__ float sm_m[kWarps], sm_l[kWarps];
     __shared__ __align__(16) float sm_acc[kWarps][D];
@@ -187,6 +193,9 @@ decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ 
     extern __shared__ float sm_w[];          // num_splits weights
     __shared__ float red[D / 32];
     __shared__ float bcast;
+    // every partial is written by the split grid, which must have completed
+    // (a no-op when launched without the programmatic attribute)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long bh = static_cast<long long>(blockIdx.y) * H + blockIdx.x;
     const float* lp = ws_lse + bh * num_splits;
     // m* = max_s lse_s
@@ -230,18 +239,33 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     const auto* k = static_cast<const __nv_bfloat16*>(a.k);
     const auto* v = static_cast<const __nv_bfloat16*>(a.v);
     auto* o = static_cast<__nv_bfloat16*>(a.o);
+    // the combine as a programmatic dependent launch of the split grid
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = g2;
+    cfg.blockDim = dim3(a.d == 64 ? 64 : 128);
+    cfg.dynamicSmemBytes = smem2;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float* ws_o = a.ws_o;
+    const float* ws_lse = a.ws_lse;
+    float* lse = a.lse;
+    const int H = a.H, ns = a.num_splits;
     if (a.d == 64) {
         decode_split_kernel<64><<<g1, kSplitThreads, 0, stream>>>(
             q, k, v, a.ws_o, a.ws_lse, a.H, a.Nk, split_len, a.num_splits, scale_log2, a.seqlens_k);
-        decode_combine_kernel<64><<<g2, 64, smem2, stream>>>(a.ws_o, a.ws_lse, o, a.lse, a.H,
-                                                             a.num_splits);
-    } else {
-        decode_split_kernel<128><<<g1, kSplitThreads, 0, stream>>>(
-            q, k, v, a.ws_o, a.ws_lse, a.H, a.Nk, split_len, a.num_splits, scale_log2, a.seqlens_k);
-        decode_combine_kernel<128><<<g2, 128, smem2, stream>>>(a.ws_o, a.ws_lse, o, a.lse, a.H,
-                                                               a.num_splits);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, ws_o, ws_lse, o, lse, H, ns);
     }
-    return cudaGetLastError();
+    decode_split_kernel<128><<<g1, kSplitThreads, 0, stream>>>(
+        q, k, v, a.ws_o, a.ws_lse, a.H, a.Nk, split_len, a.num_splits, scale_log2, a.seqlens_k);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, ws_o, ws_lse, o, lse, H, ns);
 }
 
 // ---------------------------------------------------------------------------
