@@ -53,8 +53,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # SHA-256 at capture time; reported as null when the source has changed.
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
-    # launch at the full bench workload, 1-pass ncu capture (profiles/
-    # ncu_traffic_full_size.md); valid while the kernel source is unchanged.
+    # launch at the full bench workload, 1-pass ncu capture; valid while the
+    # kernel source is unchanged.
     "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": "195b3626a3f55a77002b8c722fe2ec8e77fecb64aa32e0ae5d772e323a6faa6b",
                  "bytes_per_launch": 402933504 + 115678464,
                  "workload": "prefill_B1_H64_N8192_d128_bf16"},
@@ -284,18 +284,19 @@ def run_ours(args, rank, world, dist_on):
                 "kernel": "fwd_sm103_kernel<128>",
                 "algorithmic_flops_per_launch": fl}
 
-    # ---------------- e2e: host (pinned) inputs and outputs through the public
-    # host API, copies in and out inside the timed region, pipelined with the
-    # kernel by groups of heads
+    # ---------------- e2e: host (pinned) inputs and outputs through the C entry
+    # point attn_fwd_host, copies in and out inside the timed region,
+    # pipelined with the kernel by groups of heads
     hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
     ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     del q, k, v
-    pipe = attn.HostPipeline(w.B, w.H, w.Nq, w.Nk, w.d, device=dev, chunks=args.e2e_chunks)
+    pipe = attn.HostPipeline(w.B, w.H, w.Nq, w.Nk, w.d, device=dev, chunks=args.e2e_chunks,
+                             slots=args.e2e_slots)
 
     def e2e_step():
-        with torch.cuda.stream(stream):
-            attn.attn_fwd_from_host(hq, hk, hv, ho, hl, mask_kind=w.mask_kind, pipeline=pipe)
+        attn.attn_fwd_from_host(hq, hk, hv, ho, hl, mask_kind=w.mask_kind, pipeline=pipe,
+                                stream=stream)
 
     e_steps = max(3, args.steps // 4)
     e_total, _ = time_loop(e2e_step, e_steps, args.warmup, stream, dist_on)
@@ -305,8 +306,10 @@ def run_ours(args, rank, world, dist_on):
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
     e2e = {"value": round(fl * world * e_steps / (e_total * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": round(e_total / e_steps, 4), "api": "attn_fwd_from_host",
-           "head_groups": pipe.chunks,
+           "ms_per_step": round(e_total / e_steps, 4),
+           "api": "attn_fwd_host (C ABI; host buffers, device workspace, caller's stream)",
+           "head_groups": pipe.chunks, "device_slots": pipe.slots,
+           "gpu_launches_per_step": -(-w.B * w.H // -(-w.B * w.H // pipe.chunks)),
            "h2d_d2h_GBps": round((h2d + d2h) / (e_total / e_steps * 1e-3) / 1e9, 1)}
     # the e2e result must equal the device-resident result
     e2e["matches_device_result"] = bool(torch.equal(ho.to(dev), o))
@@ -326,7 +329,7 @@ def run_ours(args, rank, world, dist_on):
         "clocks": clk.summary(),
     })
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, x, o, args)
+        result["cpu_baseline"] = cpu_baseline(w, x, o, lse, args, args.cpu_seconds)
     del o, lse, x
     return run_sections(args, rank, world, dist_on, dev, stream, peaks, result)
 
@@ -353,10 +356,13 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
     causal = {"config": wc.describe(), "ms_per_step": round(c_total / args.steps, 4),
               "value": round(flc * world * args.steps / (c_total * 1e-3) / 1e12, 2),
               "unit": "TFLOP/s", "flop_count": "causal (visible pairs only)",
+              "gpu_launches_per_step": 1,
               "dense_equivalent_tflops": round(4.0 * wc.d * wc.B * wc.H * wc.Nq * wc.Nk * world *
                                                args.steps / (c_total * 1e-3) / 1e12, 2),
-              "frac_of_peak": round(flc / (statistics.mean(c_per) * 1e-3) / 1e12 /
-                                    peaks["bf16_tflops"], 4)}
+              "roofline": tensor_roofline(flc, c_per, peaks, "fwd_bf16_causal",
+                                          "fwd_sm103_kernel<128> (causal)")}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        causal["cpu_baseline"] = cpu_baseline(wc, xc, oc, lc, args, args.cpu_seconds / 2)
     del qc, kc, vc, oc, lc, xc
     result["causal"] = causal
     return run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result)
@@ -385,8 +391,12 @@ def run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result):
     result["masked"] = {
         "config": wm.describe(), "ms_per_step": round(m_total / args.steps, 4),
         "value": round(flm * world * args.steps / (m_total * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-        "flop_count": "visible pairs only (window and padding)",
-        "frac_of_peak": round(flm / (statistics.mean(m_per) * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)}
+        "flop_count": "visible pairs only (window and padding)", "gpu_launches_per_step": 1,
+        "roofline": tensor_roofline(flm, m_per, peaks, "fwd_bf16_masked",
+                                    "fwd_sm103_kernel<128> (window + padding)")}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["masked"]["cpu_baseline"] = cpu_baseline(wm, xm, om, lm, args,
+                                                        args.cpu_seconds / 2)
     del qm, km, vm, om, lm, xm
     return run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result)
 
@@ -507,6 +517,8 @@ def run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result):
                            "traffic": traffic_for("decode", wd.Nk / W.DECODE.Nk),
                            "algorithmic_bytes_per_step": alg_bytes,
                            "note": "time is both launches (split + combine) per step"}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        decode["cpu_baseline"] = cpu_baseline_decode(wd, xd, od, ld, args.cpu_seconds / 2)
     del qd, kd, vd, xd
     result["decode"] = decode
     return run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result)
@@ -599,43 +611,111 @@ def naive_attention_context(args, dev, stream, peaks):
     return out
 
 
+def tensor_roofline(fl, per_launch_ms, peaks, traffic_key, kernel):
+    """Roofline of a forward launch against the measured dense BF16 burst."""
+    achieved = fl / (statistics.mean(per_launch_ms) * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "traffic": traffic_for(traffic_key), "kernel": kernel,
+            "algorithmic_flops_per_launch": fl}
+
+
 # ------------------------------------------------------ oracle on the host
+def row_visible_keys(w, rows, seqlens=None):
+    """Visible keys of each flat row (b*H+h)*Nq+i under the workload's mask."""
+    rows = np.asarray(rows, np.int64)
+    i = rows % w.Nq
+    b = rows // (w.H * w.Nq)
+    L = np.full(rows.shape, w.Nk, np.int64)
+    if seqlens is not None:
+        L = np.clip(np.asarray(seqlens, np.int64)[b], 0, w.Nk)
+    hi = L.copy()
+    if w.mask_kind & (W.MASK_CAUSAL | W.MASK_WINDOW):
+        hi = np.minimum(hi, i + 1)
+    lo = np.zeros_like(i)
+    if w.mask_kind & W.MASK_WINDOW:
+        lo = np.maximum(0, i - w.window + 1)
+    return np.maximum(hi - lo, 0)
+
+
 def oracle_sample(w, x, n_rows, seed=0):
     import oracle
     orc = oracle.Oracle()
     rng = np.random.default_rng(seed)
     rows = np.sort(rng.choice(w.B * w.H * w.Nq, size=n_rows, replace=False))
     qn, kn, vn = (x[n].float().numpy() for n in ("q", "k", "v"))
+    sl = x.get("seqlens_k")
+    sl = None if sl is None else sl.numpy()
     threads = oracle.default_threads()
     t0 = time.perf_counter()
-    ro, rl = orc.attention(qn, kn, vn, w.scale, w.mask_kind, w.window, None, rows=rows,
+    ro, rl = orc.attention(qn, kn, vn, w.scale, w.mask_kind, w.window, sl, rows=rows,
                            threads=threads)
     dt = time.perf_counter() - t0
     return rows, ro, rl, dt, threads
 
 
-def cpu_baseline(w, x, o_gpu, args):
+def cpu_baseline(w, x, o_gpu, lse_gpu, args, seconds):
     """The FP64 oracle, as it stands, on a bounded sample of rows of the
-    same workload, timed on the host cores; also reports its agreement with
-    the GPU output on those rows."""
-    # calibrate on a small sample, then size the sample to ~args.cpu_seconds
+    same workload, timed on the host cores (about `seconds` of CPU work);
+    also reports its agreement with the GPU output on those rows."""
+    sl = x.get("seqlens_k")
+    sl = None if sl is None else sl.numpy()
+    # calibrate on a small sample, then size the sample to ~seconds
     rows, _, _, dt, _ = oracle_sample(w, x, 64, seed=1)
-    n = int(min(w.B * w.H * w.Nq, max(64, 64 * args.cpu_seconds / max(dt, 1e-3))))
+    n = int(min(w.B * w.H * w.Nq, max(64, 64 * seconds / max(dt, 1e-3))))
     rows, ro, rl, dt, threads = oracle_sample(w, x, n, seed=2)
-    fl = 4.0 * w.d * w.Nk * n
-    got = o_gpu.float().reshape(-1, w.d)[torch.from_numpy(rows).to(o_gpu.device)].cpu().numpy()
+    fl = 4.0 * w.d * float(row_visible_keys(w, rows, sl).sum())
+    idx = torch.from_numpy(rows).to(o_gpu.device)
+    got = o_gpu.float().reshape(-1, w.d)[idx].cpu().numpy()
+    got_l = lse_gpu.reshape(-1)[idx].cpu().double().numpy()
+    fin = np.isfinite(rl)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "%d random query rows (all %d keys each) of the prefill workload" % (n, w.Nk),
-            "max_abs_err_gpu_vs_oracle": float(np.abs(got - ro).max())}
+            "sample": "%d random query rows (each with its visible keys) of the %s workload"
+                      % (n, w.name),
+            "max_abs_err_gpu_vs_oracle": float(np.abs(got - ro).max()),
+            "max_abs_lse_err_gpu_vs_oracle": float(np.abs(got_l[fin] - rl[fin]).max())
+            if fin.any() else 0.0,
+            "lse_neginf_pattern_matches": bool(np.array_equal(np.isneginf(got_l), ~fin))}
+
+
+def cpu_baseline_decode(w, x, o_gpu, lse_gpu, seconds):
+    """The FP64 oracle on the decode workload's first heads (as many as fit in
+    about `seconds` of CPU work, every key of each), in the decode metric's
+    unit: algorithmic bytes of those heads per second."""
+    import oracle
+    orc = oracle.Oracle()
+    threads = oracle.default_threads()
+
+    def run(nh):
+        qn, kn, vn = (x[n][:, :nh].float().numpy() for n in ("q", "k", "v"))
+        t0 = time.perf_counter()
+        ro, rl = orc.attention(qn, kn, vn, w.scale, 0, 0, None, threads=threads)
+        return ro, rl, time.perf_counter() - t0
+
+    _, _, dt1 = run(1)
+    nh = int(min(w.H, max(1, seconds / max(dt1, 1e-3))))
+    ro, rl, dt = run(nh)
+    alg = 2 * w.B * nh * w.Nk * w.d * 2 + 2 * w.B * nh * w.d * 2 + w.B * nh * 4
+    got = o_gpu[:, :nh].float().cpu().numpy()
+    got_l = lse_gpu[:, :nh].cpu().double().numpy()
+    return {"value": round(alg / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "heads 0..%d of %d (all %d keys each) of the decode workload"
+                      % (nh - 1, w.H, w.Nk),
+            "max_abs_err_gpu_vs_oracle": float(np.abs(got - ro).max()),
+            "max_abs_lse_err_gpu_vs_oracle": float(np.abs(got_l - rl).max())}
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: each step a bounded sample."""
+    """The oracle as the reference arm: each of the --steps steps a bounded
+    sample of rows, sized so that all steps together take about
+    --ref-seconds of CPU work (at most --ref-seconds-per-step each)."""
     w = W.PREFILL
     x = W.generate(w)
     _, _, _, dt0, _ = oracle_sample(w, x, 32, seed=1)
-    n = int(max(32, 32 * args.ref_seconds_per_step / max(dt0, 1e-3)))
+    per_step = min(args.ref_seconds_per_step, args.ref_seconds / max(args.steps, 1))
+    n = int(max(8, 32 * per_step / max(dt0, 1e-3)))
     for s in range(args.warmup):
         oracle_sample(w, x, min(n, 64), seed=100 + s)
     total = 0.0
@@ -665,8 +745,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds-per-step", type=float, default=6.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="CPU seconds the reference arm's timed steps take in all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=16, help="head groups of the e2e pipeline")
+    ap.add_argument("--e2e-slots", type=int, default=3, help="device buffer sets of the e2e pipeline")
     # profiling helpers: run one section, or a reduced size of it
     ap.add_argument("--no-naive", action="store_true",
                     help="skip the naive (score matrix in HBM) attention context measurement")
@@ -684,7 +767,6 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        args.steps = min(args.steps, 3)
         print(json.dumps(run_reference(args, rank, world)))
         return
     dist_on = world > 1

@@ -43,6 +43,11 @@
  *   - Ownership: the caller allocates every buffer (including the decode
  *     workspace); the library allocates no device memory on these paths and
  *     keeps no state between calls except a per-device error word.
+ *   - The library looks up the device addresses of its own device variables
+ *     (the error word, and the fixed array of attn_decode_splitkv_noalloc)
+ *     once per device and keeps them for the life of the process. Resetting
+ *     a device (cudaDeviceReset) or destroying its primary context while the
+ *     library is loaded makes those addresses stale; that is not supported.
  *   - Calls are asynchronous and stream-ordered on `stream` (0 = legacy
  *     default stream). Argument errors are reported synchronously by the
  *     return value, with a message in attn_last_error(); the outputs are then
@@ -115,6 +120,66 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v,
                        int B, int H, int Nq, int Nk, int d, float scale,
                        int mask_kind, int window, const int* seqlens_k,
                        attn_stream_t stream);
+
+/*
+ * attn_fwd_host_workspace_bytes -- size in bytes of the device workspace that
+ * attn_fwd_host needs: min(slots, number of groups) buffer sets, each
+ * holding q, k, v, o (BF16) and lse (FP32) for ceil(B*H / groups) heads,
+ * plus the per-head key lengths, at 256-byte-aligned offsets. Returns 0 for
+ * invalid arguments (negative sizes, d not in {64, 128}, groups < 1, slots
+ * outside [1, 8]).
+ */
+size_t attn_fwd_host_workspace_bytes(int B, int H, int Nq, int Nk, int d, int groups,
+                                     int slots);
+
+/*
+ * attn_fwd_host -- attn_fwd for inputs and outputs in HOST memory.
+ *
+ * Only Q, K, V and O cross device memory in the fused method (P1 "Derive
+ * online softmax, ...", "A strong answer", the cost paragraph); this call
+ * moves exactly those across the host link, overlapped with the kernel. The
+ * B*H heads are cut into `groups` contiguous groups of ceil(B*H / groups)
+ * heads; group g is copied into buffer set g % slots of the workspace (one
+ * cudaMemcpyAsync per tensor), computed by the attn_fwd kernel on that
+ * slot's stream, and its o and lse copied back, so that the copy-in of one
+ * group, the kernel of the next and the copy-out of the previous run at the
+ * same time. A slot is refilled once its previous group has been copied
+ * out. The result is bit for bit that of attn_fwd on the same values.
+ *
+ *   q, k, v      HOST BF16 pointers, [B,H,Nq,d] and [B,H,Nk,d], 2-byte
+ *                aligned. Page-locked memory (cudaHostAlloc /
+ *                cudaHostRegister) is needed for the copies to overlap the
+ *                kernels; pageable memory works but serialises them.
+ *   o            HOST BF16 [B,H,Nq,d] (written).
+ *   lse          HOST FP32 [B,H,Nq] (written), or NULL.
+ *   B..window    as attn_fwd.
+ *   seqlens_k    HOST int32 [B], required iff ATTN_MASK_PADDING is set.
+ *   groups       number of head groups, >= 1 (more than B*H acts as B*H).
+ *   slots        device buffer sets in flight, 1..8 (3 keeps the copy-in
+ *                stream busy on a ~200 GB/s host link).
+ *   workspace    caller-owned DEVICE buffer of at least
+ *                attn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, groups,
+ *                slots) bytes, 256-byte aligned; overwritten. Two calls that
+ *                share a workspace must be ordered on one stream.
+ *   stream       the caller's stream: the copies and kernels start after the
+ *                work already queued on it, and work queued on it after this
+ *                call starts once o and lse are in host memory. The call
+ *                returns once everything is queued; synchronise `stream`
+ *                before reading o or lse, and keep every host buffer,
+ *                seqlens_k included, alive and unmodified until then.
+ * The library creates, on the first call on a device, two copy streams,
+ * eight compute streams and their events, and keeps them for the life of
+ * the process; calls on one device are queued one at a time. No device
+ * memory is allocated. Errors: as attn_fwd, plus ATTN_ERR_INVALID_ARG for a
+ * missing or short workspace or bad groups/slots; a CUDA error while
+ * queueing returns ATTN_ERR_CUDA with part of the work queued.
+ */
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v,
+                            void* o, float* lse,
+                            int B, int H, int Nq, int Nk, int d, float scale,
+                            int mask_kind, int window, const int* seqlens_k,
+                            int groups, int slots, void* workspace, size_t workspace_bytes,
+                            attn_stream_t stream);
 
 /*
  * attn_fwd_fp8 -- attn_fwd with 8-bit floating-point inputs, the FP8 mode P1

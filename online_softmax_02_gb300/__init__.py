@@ -10,8 +10,10 @@ raises.
 Functions (same names as the C entry points):
   attn_fwd(q, k, v, ...)            BF16 fused forward -> (o, lse)
   attn_fwd_f32(q, k, v, ...)        FP32 fused forward -> (o, lse)
-  attn_fwd_from_host(q, k, v, o, ...)  BF16 forward on host tensors, copies
-                                    pipelined with the kernel by head groups
+  attn_fwd_from_host(q, k, v, o, ...)  BF16 forward on host tensors through
+                                    attn_fwd_host (copies pipelined with the
+                                    kernel by head groups)
+  attn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, groups, slots)
   attn_bwd(q, k, v, o, dout, lse, ...)  backward -> (dq, dk, dv)
   attn_bwd_workspace_bytes(B, H, Nq, d)
   attn_decode_workspace_bytes(B, H, d, num_splits)
@@ -57,12 +59,30 @@ def load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libattn.so not found at %s: build it with "
                           "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
-    lib = ctypes.CDLL(LIB_PATH)
+    _lib = _configure(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def open_build(path: str):
+    """Load another build of libattn.so -- one compiled with compile-time
+    options other than the defaults (``build.build(out=..., extra_flags=...)``)
+    -- and return its ctypes handle; pass it as ``lib=`` to attn_fwd or
+    attn_fwd_fp8. The default library is not affected."""
+    if not os.path.exists(path):
+        raise ImportError("no library at %s" % path)
+    return _configure(ctypes.CDLL(path))
+
+
+def _configure(lib):
     P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, P]
     lib.attn_fwd.restype = I
     lib.attn_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, P]
     lib.attn_fwd_f32.restype = I
+    lib.attn_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    lib.attn_fwd_host_workspace_bytes.restype = S
+    lib.attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, I, I, P, S, P]
+    lib.attn_fwd_host.restype = I
     lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, F, F, I, I, P, P]
     lib.attn_fwd_fp8.restype = I
     lib.attn_decode_workspace_bytes.argtypes = [I, I, I, I]
@@ -87,13 +107,12 @@ def load():
     lib.attn_last_error.restype = ctypes.c_char_p
     lib.attn_version.argtypes = []
     lib.attn_version.restype = ctypes.c_char_p
-    _lib = lib
     return lib
 
 
-def _check(status: int):
+def _check(status: int, lib=None):
     if status != ATTN_OK:
-        raise AttnError(status, load().attn_last_error().decode())
+        raise AttnError(status, (lib or load()).attn_last_error().decode())
 
 
 def _ptr(t):
@@ -120,7 +139,7 @@ def _require(t, name, dtype, device=None):
 
 
 def _fwd(fn, dtype, q, k, v, o, lse, scale, mask_kind, window, seqlens_k, stream,
-         out_dtype=None, descales=()):
+         out_dtype=None, descales=(), lib=None):
     import torch
     out_dtype = dtype if out_dtype is None else out_dtype
     _require(q, "q", dtype)
@@ -152,26 +171,28 @@ def _fwd(fn, dtype, q, k, v, o, lse, scale, mask_kind, window, seqlens_k, stream
         st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                 float(scale), *[float(f) for f in descales], int(mask_kind), int(window),
                 _ptr(seqlens_k), _stream_handle(stream, dev))
-    _check(st)
+    _check(st, lib)
     return o, lse
 
 
 def attn_fwd(q, k, v, o=None, lse=None, scale=None, mask_kind=MASK_NONE, window=0,
-             seqlens_k=None, stream=None, want_lse=True):
+             seqlens_k=None, stream=None, want_lse=True, lib=None):
     """BF16 fused attention forward through ``attn_fwd``.
 
     q [B,H,Nq,d], k/v [B,H,Nk,d] contiguous BF16 CUDA tensors; returns
     (o [B,H,Nq,d] BF16, lse [B,H,Nq] FP32 or None). Output buffers may be
-    passed in to avoid allocation."""
+    passed in to avoid allocation. ``lib``: a handle from ``open_build``
+    (default: the library next to this file)."""
     import torch
     if lse is None and want_lse:
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    return _fwd(load().attn_fwd, torch.bfloat16, q, k, v, o, lse, scale, mask_kind,
-                window, seqlens_k, stream)
+    return _fwd((lib or load()).attn_fwd, torch.bfloat16, q, k, v, o, lse, scale, mask_kind,
+                window, seqlens_k, stream, lib=lib)
 
 
 def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, o=None, lse=None, scale=None,
-                 mask_kind=MASK_NONE, window=0, seqlens_k=None, stream=None, want_lse=True):
+                 mask_kind=MASK_NONE, window=0, seqlens_k=None, stream=None, want_lse=True,
+                 lib=None):
     """E4M3 fused attention forward through ``attn_fwd_fp8``.
 
     q [B,H,Nq,128], k/v [B,H,Nk,128] contiguous ``torch.float8_e4m3fn`` CUDA
@@ -180,9 +201,9 @@ def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, o=None, lse=None, sca
     import torch
     if lse is None and want_lse:
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    return _fwd(load().attn_fwd_fp8, torch.float8_e4m3fn, q, k, v, o, lse, scale, mask_kind,
-                window, seqlens_k, stream, out_dtype=torch.bfloat16,
-                descales=(descale_q, descale_k, descale_v))
+    return _fwd((lib or load()).attn_fwd_fp8, torch.float8_e4m3fn, q, k, v, o, lse, scale,
+                mask_kind, window, seqlens_k, stream, out_dtype=torch.bfloat16,
+                descales=(descale_q, descale_k, descale_v), lib=lib)
 
 
 def attn_fwd_f32(q, k, v, o=None, lse=None, scale=None, mask_kind=MASK_NONE, window=0,
@@ -245,6 +266,24 @@ def attn_decode_workspace_bytes(B: int, H: int, d: int, num_splits: int) -> int:
     return int(load().attn_decode_workspace_bytes(B, H, d, num_splits))
 
 
+def _check_decode_aux(o, q, lse, seqlens_k, B, H, dev):
+    """Shapes of the decode outputs and key lengths: the C entry points see
+    only pointers, so a short lse or seqlens_k would be written or read past
+    its end by the kernels."""
+    import torch
+    _require(o, "o", torch.bfloat16, dev)
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape [B, H, 1, d]")
+    if lse is not None:
+        _require(lse, "lse", torch.float32, dev)
+        if lse.numel() != B * H or (lse.dim() == 3 and tuple(lse.shape) != (B, H, 1)):
+            raise ValueError("lse must be [B, H, 1] (B*H FP32 values)")
+    if seqlens_k is not None:
+        _require(seqlens_k, "seqlens_k", torch.int32, dev)
+        if tuple(seqlens_k.shape) != (B,):
+            raise ValueError("seqlens_k must be [B]")
+
+
 def attn_decode_splitkv(q, k, v, o=None, lse=None, scale=None, seqlens_k=None,
                         num_splits=64, workspace=None, stream=None, want_lse=True):
     """Split-KV decode through ``attn_decode_splitkv``: q [B,H,1,d], k/v
@@ -264,13 +303,9 @@ def attn_decode_splitkv(q, k, v, o=None, lse=None, scale=None, seqlens_k=None,
         raise ValueError("k and v must be [B, H, Nk, d]")
     if o is None:
         o = torch.empty_like(q)
-    _require(o, "o", torch.bfloat16, dev)
     if lse is None and want_lse:
         lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
-    if lse is not None:
-        _require(lse, "lse", torch.float32, dev)
-    if seqlens_k is not None:
-        _require(seqlens_k, "seqlens_k", torch.int32, dev)
+    _check_decode_aux(o, q, lse, seqlens_k, B, H, dev)
     need = int(lib.attn_decode_workspace_bytes(B, H, d, num_splits))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
@@ -307,13 +342,7 @@ def attn_decode_splitkv_noalloc(q, k, v, o, lse=None, scale=None, seqlens_k=None
     Nk = k.shape[2]
     if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
         raise ValueError("k and v must be [B, H, Nk, d]")
-    _require(o, "o", torch.bfloat16, dev)
-    if tuple(o.shape) != tuple(q.shape):
-        raise ValueError("o must have q's shape")
-    if lse is not None:
-        _require(lse, "lse", torch.float32, dev)
-    if seqlens_k is not None:
-        _require(seqlens_k, "seqlens_k", torch.int32, dev)
+    _check_decode_aux(o, q, lse, seqlens_k, B, H, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(dev):
@@ -324,121 +353,85 @@ def attn_decode_splitkv_noalloc(q, k, v, o, lse=None, scale=None, seqlens_k=None
     return o, lse
 
 
+def attn_fwd_host_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, groups: int = 16,
+                                  slots: int = 3) -> int:
+    return int(load().attn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, groups, slots))
+
+
 class HostPipeline:
-    """Reusable device buffers and streams for ``attn_fwd_from_host``.
+    """The device workspace of ``attn_fwd_host`` for one shape, kept so that
+    repeated calls allocate nothing: ``slots`` buffer sets (q, k, v, o, lse)
+    of ceil(B*H / chunks) heads each. Create it once for a shape and reuse it
+    across calls ordered on one stream."""
 
-    Holds, per in-flight chunk slot, device buffers for q, k, v, o and lse
-    and a compute stream, plus one copy-in and one copy-out stream. Create it
-    once for a shape and reuse it across calls. With three slots (the
-    default) the copy-in of group i waits only for the copy-out of group
-    i - 3, which has long finished: the copy-in stream, the bottleneck on a
-    host link of about 200 GB/s, never stalls (two slots measured 852 and
-    three 918 TFLOP/s end to end on the prefill shape in 16 head groups)."""
-
-    def __init__(self, B, H, Nq, Nk, d, device=None, chunks=4, dtype=None, slots=3):
+    def __init__(self, B, H, Nq, Nk, d, device=None, chunks=16, slots=3):
         import torch
-        dtype = torch.bfloat16 if dtype is None else dtype
         self.device = torch.device("cuda") if device is None else torch.device(device)
-        self.BH, self.Nq, self.Nk, self.d = B * H, Nq, Nk, d
-        self.B, self.H = B, H
-        self.chunks = max(1, min(int(chunks), self.BH))
-        self.per = -(-self.BH // self.chunks)
-        nslot = max(1, min(int(slots), self.chunks))
-        mk = lambda n: torch.empty((self.per, n, d), dtype=dtype, device=self.device)
-        self.slots = [dict(q=mk(Nq), k=mk(Nk), v=mk(Nk), o=mk(Nq),
-                           lse=torch.empty((self.per, Nq), dtype=torch.float32, device=self.device))
-                      for _ in range(nslot)]
-        self.s_in = torch.cuda.Stream(self.device)
-        # one compute stream per slot: a group's kernel can start on SMs that
-        # the previous group's last wave has already left
-        self.s_run = [torch.cuda.Stream(self.device) for _ in self.slots]
-        self.s_out = torch.cuda.Stream(self.device)
+        self.B, self.H, self.Nq, self.Nk, self.d = B, H, Nq, Nk, d
+        self.chunks, self.slots = int(chunks), int(slots)
+        need = attn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, self.chunks, self.slots)
+        if need == 0 and B * H > 0:
+            raise ValueError("invalid host pipeline arguments")
+        self.workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=self.device)
+
+
+def _require_host(t, name, dtype):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("%s must be a CPU tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
 
 
 def attn_fwd_from_host(q, k, v, o, lse=None, scale=None, mask_kind=MASK_NONE, window=0,
-                       seqlens_k=None, pipeline=None, chunks=4):
-    """Fused attention forward for inputs and outputs in (pinned) host memory.
+                       seqlens_k=None, pipeline=None, chunks=16, slots=3, stream=None):
+    """Fused attention forward for inputs and outputs in host memory, through
+    ``attn_fwd_host``.
 
-    q [B,H,Nq,d], k/v [B,H,Nk,d] and o [B,H,Nq,d] are CPU tensors (pin them
-    for asynchronous copies; BF16); lse optional CPU FP32 [B,H,Nq]. The
-    (b, h) heads are cut into ``chunks`` contiguous groups: the host-to-device
-    copy of group i+1 and the device-to-host copy of group i-1 overlap the
-    ``attn_fwd`` kernel on group i (device buffer slots, three by default,
-    each with its own compute stream, plus a copy-in and a copy-out stream).
-    Returns after the last copy back has been queued; the caller's current
-    stream is made to wait for it, so synchronising that stream (or the
-    device) makes o / lse readable. seqlens_k (padding mask) is a CPU int32
-    [B] tensor.
-    """
+    q [B,H,Nq,d], k/v [B,H,Nk,d] and o [B,H,Nq,d] are BF16 CPU tensors (pin
+    them, e.g. ``.pin_memory()``, for the copies to overlap the kernels); lse
+    an optional FP32 CPU [B,H,Nq]; seqlens_k a CPU int32 [B] (padding mask).
+    The heads are cut into ``chunks`` groups whose copy-in, kernel and
+    copy-out overlap (``slots`` device buffer sets; ``pipeline`` holds a
+    reusable workspace). Returns once the work is queued on ``stream`` (the
+    current stream by default); synchronise it before reading o / lse."""
     import torch
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _require_host(t, n, torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, Nq, d]")
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d] matching q")
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape")
+    if lse is not None:
+        _require_host(lse, "lse", torch.float32)
+        if tuple(lse.shape) != (B, H, Nq):
+            raise ValueError("lse must be [B, H, Nq]")
+    if seqlens_k is not None:
+        _require_host(seqlens_k, "seqlens_k", torch.int32)
+        if tuple(seqlens_k.shape) != (B,):
+            raise ValueError("seqlens_k must be [B]")
     if pipeline is None:
         pipeline = HostPipeline(B, H, Nq, Nk, d, device=torch.cuda.current_device(),
-                                chunks=chunks, dtype=q.dtype)
+                                chunks=chunks, slots=slots)
     P = pipeline
-    if (P.BH, P.Nq, P.Nk, P.d) != (B * H, Nq, Nk, d):
+    if (P.B * P.H, P.Nq, P.Nk, P.d) != (B * H, Nq, Nk, d):
         raise ValueError("pipeline was built for another shape")
-    qf, kf, vf, of = (t.reshape(B * H, -1, d) for t in (q, k, v, o))
-    lf = lse.reshape(B * H, Nq) if lse is not None else None
-    sl_dev = None
-    if seqlens_k is not None:
-        # one key length per (b, h) so that any group of heads is a batch
-        sl_dev = seqlens_k.to(torch.int32).repeat_interleave(H).to(P.device, non_blocking=True)
-    # the pipeline's streams start after the caller's stream (inputs ready)
-    caller = torch.cuda.current_stream(P.device)
-    P.s_in.wait_stream(caller)
-    for st in P.s_run:
-        st.wait_stream(caller)
-    ev_in = [torch.cuda.Event() for _ in P.slots]
-    ev_run = [torch.cuda.Event() for _ in P.slots]
-    ev_out = [torch.cuda.Event() for _ in P.slots]
-    started = [False] * len(P.slots)
-    for c in range(P.chunks):
-        a, b = c * P.per, min((c + 1) * P.per, B * H)
-        if a >= b:
-            break
-        n = b - a
-        si = c % len(P.slots)
-        S = P.slots[si]
-        with torch.cuda.stream(P.s_in):
-            if started[si]:
-                P.s_in.wait_event(ev_out[si])      # slot's previous results copied out
-            S["q"][:n].copy_(qf[a:b], non_blocking=True)
-            S["k"][:n].copy_(kf[a:b], non_blocking=True)
-            S["v"][:n].copy_(vf[a:b], non_blocking=True)
-            ev_in[si].record(P.s_in)
-        run = P.s_run[si]
-        with torch.cuda.stream(run):
-            run.wait_event(ev_in[si])
-            if sl_dev is None:
-                attn_fwd(S["q"][:n].unsqueeze(0), S["k"][:n].unsqueeze(0),
-                         S["v"][:n].unsqueeze(0), o=S["o"][:n].unsqueeze(0),
-                         lse=S["lse"][:n].unsqueeze(0) if lf is not None else None,
-                         scale=scale, mask_kind=mask_kind, window=window,
-                         stream=run, want_lse=lf is not None)
-            else:
-                _fwd_heads_padded(S, n, sl_dev[a:b], lf is not None, scale, mask_kind, window,
-                                  run)
-            ev_run[si].record(run)
-        with torch.cuda.stream(P.s_out):
-            P.s_out.wait_event(ev_run[si])
-            of[a:b].copy_(S["o"][:n], non_blocking=True)
-            if lf is not None:
-                lf[a:b].copy_(S["lse"][:n], non_blocking=True)
-            ev_out[si].record(P.s_out)
-        started[si] = True
-    caller.wait_stream(P.s_out)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(P.device):
+        st = lib.attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                               float(scale), int(mask_kind), int(window), _ptr(seqlens_k),
+                               P.chunks, P.slots, _ptr(P.workspace), P.workspace.numel(),
+                               _stream_handle(stream, P.device))
+    _check(st)
     return o, lse
-
-
-def _fwd_heads_padded(S, n, sl, want_lse, scale, mask_kind, window, stream):
-    """A group of n heads as a batch of n one-head problems, so that each
-    head carries its own key length."""
-    q, k, v, o = (S[x][:n].unsqueeze(1) for x in ("q", "k", "v", "o"))
-    lse = S["lse"][:n].unsqueeze(1) if want_lse else None
-    return attn_fwd(q, k, v, o=o, lse=lse, scale=scale, mask_kind=mask_kind, window=window,
-                    seqlens_k=sl.contiguous(), stream=stream, want_lse=want_lse)
 
 
 def attn_softmax_rows(x, y=None, lse=None, stream=None, want_lse=True):
@@ -464,11 +457,12 @@ def attn_softmax_rows(x, y=None, lse=None, stream=None, want_lse=True):
     return y, lse
 
 
-def attn_check_device_error(stream=None):
+def attn_check_device_error(stream=None, lib=None):
     """Synchronise and raise AttnError if a kernel gave up a bounded wait."""
     import torch
     h = _stream_handle(stream, torch.cuda.current_device()) if stream is not None else None
-    _check(load().attn_check_device_error(h))
+    lib = lib or load()
+    _check(lib.attn_check_device_error(h), lib)
 
 
 def attn_exp2_soft(x, y=None, stream=None):

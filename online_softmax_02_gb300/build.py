@@ -36,14 +36,21 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if needed) and return the path of libattn.so."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str | None = None,
+          build_dir: str | None = None) -> str:
+    """Compile (if needed) and return the path of libattn.so.
+
+    ``extra_flags`` are added to every nvcc compile; a build with compile-time
+    options other than the defaults goes to its own ``out`` library and
+    ``build_dir`` (the default build stays untouched)."""
+    LIB_OUT = LIB if out is None else out
+    BUILD_DIR = BUILD if build_dir is None else build_dir
+    os.makedirs(BUILD_DIR, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "attn.h")]
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, [s, *hdrs]):
             cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-c", s, "-o", obj]
@@ -61,12 +68,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         for out in ex.map(run, jobs):
             if verbose and out:
                 print(out)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    if force or jobs or _stale(LIB_OUT, objs):
+        tmp = LIB_OUT + ".tmp%d" % os.getpid()
         run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt",
              "-lpthread"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, LIB_OUT)
+    return LIB_OUT
 
 
 if __name__ == "__main__":

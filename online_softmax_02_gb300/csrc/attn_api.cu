@@ -46,6 +46,7 @@ attn_status_t cuda_fail(cudaError_t e, const char* what) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Device address of the error word on the current device (cached per device).
 attn_status_t err_word(unsigned int** out) {
@@ -165,21 +166,11 @@ attn_status_t check_fwd(const void* q, const void* k, const void* v, const void*
     return ATTN_OK;
 }
 
-}  // namespace
-}  // namespace attn
-
-using namespace attn;
-
-ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                                int B, int H, int Nq, int Nk, int d, float scale, int mask_kind,
-                                int window, const int* seqlens_k, attn_stream_t stream) {
-    bool nothing = false;
-    attn_status_t st = check_fwd(q, k, v, o, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k,
-                                 &nothing);
-    if (st != ATTN_OK || nothing) return st;
-    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
-        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// The BF16 forward on device buffers, after the argument checks.
+attn_status_t fwd_bf16_launch(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int Nq, int Nk, int d, float scale, int mask_kind,
+                              int window, const int* seqlens_k, cudaStream_t s) {
+    attn_status_t st;
     const long long rows = static_cast<long long>(B) * H * Nq;
     if (Nk == 0) {
         cudaError_t e = launch_fill_empty(o, lse, rows, d, true, s);
@@ -196,6 +187,227 @@ ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, voi
     FwdArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k, err};
     cudaError_t e = launch_fwd_sm103_maps(a, tq, tk, tv, to, s);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd kernel launch");
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+ATTN_API attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int Nq, int Nk, int d, float scale, int mask_kind,
+                                int window, const int* seqlens_k, attn_stream_t stream) {
+    bool nothing = false;
+    attn_status_t st = check_fwd(q, k, v, o, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k,
+                                 &nothing);
+    if (st != ATTN_OK || nothing) return st;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    return fwd_bf16_launch(q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k,
+                           static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// attn_fwd_host: the forward on host-resident inputs and outputs.
+//
+// The (b, h) heads are cut into contiguous groups; each group is copied into
+// one of `slots` device buffer sets of the caller's workspace, computed by the
+// same kernel as attn_fwd, and copied back, so that the copy-in of one group,
+// the kernel of another and the copy-out of a third overlap (only Q, K, V and
+// O cross the host link, as only they cross HBM in the fused method).
+// Streams and events are the library's own, created once per device.
+// ---------------------------------------------------------------------------
+namespace attn {
+namespace {
+
+constexpr int kMaxHostSlots = 8;
+
+struct HostLayout {
+    long long bh = 0, per = 0, groups = 0;
+    int slots = 0;
+    size_t q = 0, kv = 0, o = 0, lse = 0, slot = 0, lens = 0, total = 0;
+};
+
+bool host_layout(int B, int H, int Nq, int Nk, int d, int groups, int slots, HostLayout* L) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || (d != 64 && d != 128) || groups < 1 ||
+        slots < 1 || slots > kMaxHostSlots)
+        return false;
+    L->bh = static_cast<long long>(B) * H;
+    if (L->bh == 0) return true;
+    const long long g = std::min<long long>(groups, L->bh);
+    L->per = (L->bh + g - 1) / g;
+    L->groups = (L->bh + L->per - 1) / L->per;
+    L->slots = static_cast<int>(std::min<long long>(slots, L->groups));
+    const size_t per = static_cast<size_t>(L->per);
+    L->q = align256(per * Nq * d * 2);
+    L->kv = align256(per * Nk * d * 2);
+    L->o = L->q;
+    L->lse = align256(per * Nq * sizeof(float));
+    L->slot = L->q + 2 * L->kv + L->o + L->lse;
+    L->lens = align256(static_cast<size_t>(L->bh) * sizeof(int) + static_cast<size_t>(B) * sizeof(int));
+    L->total = L->slots * L->slot + L->lens;
+    return true;
+}
+
+// The library's copy and compute streams and their events on one device.
+struct HostStreams {
+    std::mutex mu;                       // one enqueue at a time per device
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr, run[kMaxHostSlots] = {};
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t ev_in[kMaxHostSlots] = {}, ev_run[kMaxHostSlots] = {}, ev_out[kMaxHostSlots] = {};
+};
+
+attn_status_t host_streams(HostStreams** out) {
+    static std::mutex create_mu;
+    static HostStreams per_device[128];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 128) return fail(ATTN_ERR_UNSUPPORTED, "device index %d", dev);
+    HostStreams& h = per_device[dev];
+    std::lock_guard<std::mutex> lock(create_mu);
+    if (!h.ready) {
+        auto mk_s = [](cudaStream_t* s) { return cudaStreamCreateWithFlags(s, cudaStreamNonBlocking); };
+        auto mk_e = [](cudaEvent_t* ev) { return cudaEventCreateWithFlags(ev, cudaEventDisableTiming); };
+        if ((e = mk_s(&h.in)) != cudaSuccess || (e = mk_s(&h.out)) != cudaSuccess ||
+            (e = mk_e(&h.start)) != cudaSuccess || (e = mk_e(&h.done)) != cudaSuccess)
+            return cuda_fail(e, "creating the host pipeline's streams");
+        for (int i = 0; i < kMaxHostSlots; ++i)
+            if ((e = mk_s(&h.run[i])) != cudaSuccess || (e = mk_e(&h.ev_in[i])) != cudaSuccess ||
+                (e = mk_e(&h.ev_run[i])) != cudaSuccess || (e = mk_e(&h.ev_out[i])) != cudaSuccess)
+                return cuda_fail(e, "creating the host pipeline's streams");
+        h.ready = true;
+    }
+    *out = &h;
+    return ATTN_OK;
+}
+
+// lens[b * H + h] = seqlens_k[b]: one key length per head, so that any group
+// of heads is a batch of one-head problems.
+__global__ void expand_seqlens_kernel(const int* __restrict__ src, int* __restrict__ dst,
+                                      long long bh, int H) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < bh;
+         i += (long long)gridDim.x * blockDim.x)
+        dst[i] = src[i / H];
+}
+
+}  // namespace
+}  // namespace attn
+
+ATTN_API size_t attn_fwd_host_workspace_bytes(int B, int H, int Nq, int Nk, int d, int groups,
+                                              int slots) {
+    HostLayout L;
+    if (!host_layout(B, H, Nq, Nk, d, groups, slots, &L)) return 0;
+    return L.total;
+}
+
+ATTN_API attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                                     int mask_kind, int window, const int* seqlens_k, int groups,
+                                     int slots, void* workspace, size_t workspace_bytes,
+                                     attn_stream_t stream) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d Nq=%d Nk=%d)", B, H, Nq, Nk);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+    if (mask_kind & ~(ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW | ATTN_MASK_PADDING))
+        return fail(ATTN_ERR_INVALID_ARG, "unknown mask bits 0x%x", mask_kind);
+    if ((mask_kind & ATTN_MASK_WINDOW) && window < 1)
+        return fail(ATTN_ERR_INVALID_ARG, "window must be >= 1 with ATTN_MASK_WINDOW");
+    const bool padded = (mask_kind & ATTN_MASK_PADDING) != 0;
+    if (padded != (seqlens_k != nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "seqlens_k must be given iff ATTN_MASK_PADDING is set");
+    if (groups < 1) return fail(ATTN_ERR_INVALID_ARG, "groups must be >= 1");
+    if (slots < 1 || slots > kMaxHostSlots)
+        return fail(ATTN_ERR_INVALID_ARG, "slots must be in [1, %d]", kMaxHostSlots);
+    HostLayout L;
+    host_layout(B, H, Nq, Nk, d, groups, slots, &L);
+    if (L.bh == 0 || Nq == 0) return ATTN_OK;
+    if (L.per > 65535) return fail(ATTN_ERR_UNSUPPORTED, "more than 65535 heads per group");
+    if (q == nullptr || o == nullptr || (Nk > 0 && (k == nullptr || v == nullptr)))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must not be NULL");
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 1u)
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 2-byte aligned");
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    if (workspace == nullptr || workspace_bytes < L.total)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", L.total,
+                    workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+
+    HostStreams* hs = nullptr;
+    attn_status_t st = host_streams(&hs);
+    if (st != ATTN_OK) return st;
+    std::lock_guard<std::mutex> lock(hs->mu);
+    cudaStream_t caller = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+#define ATTN_HOST_CHECK(call, what)                          \
+    do {                                                     \
+        if ((e = (call)) != cudaSuccess) return cuda_fail(e, what); \
+    } while (0)
+    // every stream of the pipeline starts after the work queued on the caller's
+    ATTN_HOST_CHECK(cudaEventRecord(hs->start, caller), "cudaEventRecord");
+    ATTN_HOST_CHECK(cudaStreamWaitEvent(hs->in, hs->start, 0), "cudaStreamWaitEvent");
+    ATTN_HOST_CHECK(cudaStreamWaitEvent(hs->out, hs->start, 0), "cudaStreamWaitEvent");
+    for (int i = 0; i < L.slots; ++i)
+        ATTN_HOST_CHECK(cudaStreamWaitEvent(hs->run[i], hs->start, 0), "cudaStreamWaitEvent");
+
+    char* ws = static_cast<char*>(workspace);
+    int* lens = reinterpret_cast<int*>(ws + L.slots * L.slot);       // [B*H], then [B]
+    if (padded) {
+        int* lens_b = lens + L.bh;
+        ATTN_HOST_CHECK(cudaMemcpyAsync(lens_b, seqlens_k, sizeof(int) * B, cudaMemcpyHostToDevice,
+                                        hs->in), "copy of seqlens_k");
+        const int blocks = static_cast<int>(std::min<long long>((L.bh + 255) / 256, 1024));
+        expand_seqlens_kernel<<<blocks, 256, 0, hs->in>>>(lens_b, lens, L.bh, H);
+        ATTN_HOST_CHECK(cudaGetLastError(), "seqlens kernel launch");
+    }
+    const size_t qrow = static_cast<size_t>(Nq) * d * 2, krow = static_cast<size_t>(Nk) * d * 2;
+    for (long long c = 0; c < L.groups; ++c) {
+        const long long a = c * L.per, n = std::min(L.per, L.bh - a);
+        const int si = static_cast<int>(c % L.slots);
+        char* sq = ws + si * L.slot;
+        char* sk = sq + L.q;
+        char* sv = sk + L.kv;
+        char* so = sv + L.kv;
+        float* sl = reinterpret_cast<float*>(so + L.o);
+        if (c >= L.slots)   // the slot's previous group has been copied out
+            ATTN_HOST_CHECK(cudaStreamWaitEvent(hs->in, hs->ev_out[si], 0), "cudaStreamWaitEvent");
+        ATTN_HOST_CHECK(cudaMemcpyAsync(sq, static_cast<const char*>(q) + a * qrow, n * qrow,
+                                        cudaMemcpyHostToDevice, hs->in), "copy of q");
+        if (krow > 0) {
+            ATTN_HOST_CHECK(cudaMemcpyAsync(sk, static_cast<const char*>(k) + a * krow, n * krow,
+                                            cudaMemcpyHostToDevice, hs->in), "copy of k");
+            ATTN_HOST_CHECK(cudaMemcpyAsync(sv, static_cast<const char*>(v) + a * krow, n * krow,
+                                            cudaMemcpyHostToDevice, hs->in), "copy of v");
+        }
+        ATTN_HOST_CHECK(cudaEventRecord(hs->ev_in[si], hs->in), "cudaEventRecord");
+        cudaStream_t run = hs->run[si];
+        ATTN_HOST_CHECK(cudaStreamWaitEvent(run, hs->ev_in[si], 0), "cudaStreamWaitEvent");
+        // the group as H = n heads of one batch, or, with padding, as n
+        // one-head batches carrying their own key lengths
+        st = fwd_bf16_launch(sq, sk, sv, so, lse != nullptr ? sl : nullptr,
+                             padded ? static_cast<int>(n) : 1, padded ? 1 : static_cast<int>(n),
+                             Nq, Nk, d, scale, mask_kind, window, padded ? lens + a : nullptr, run);
+        if (st != ATTN_OK) return st;
+        ATTN_HOST_CHECK(cudaEventRecord(hs->ev_run[si], run), "cudaEventRecord");
+        ATTN_HOST_CHECK(cudaStreamWaitEvent(hs->out, hs->ev_run[si], 0), "cudaStreamWaitEvent");
+        ATTN_HOST_CHECK(cudaMemcpyAsync(static_cast<char*>(o) + a * qrow, so, n * qrow,
+                                        cudaMemcpyDeviceToHost, hs->out), "copy of o");
+        if (lse != nullptr)
+            ATTN_HOST_CHECK(cudaMemcpyAsync(lse + a * Nq, sl, n * Nq * sizeof(float),
+                                            cudaMemcpyDeviceToHost, hs->out), "copy of lse");
+        ATTN_HOST_CHECK(cudaEventRecord(hs->ev_out[si], hs->out), "cudaEventRecord");
+    }
+    // the caller's stream continues once the last copy back has landed
+    ATTN_HOST_CHECK(cudaEventRecord(hs->done, hs->out), "cudaEventRecord");
+    ATTN_HOST_CHECK(cudaStreamWaitEvent(caller, hs->done, 0), "cudaStreamWaitEvent");
+#undef ATTN_HOST_CHECK
+    return ATTN_OK;
 }
 
 ATTN_API attn_status_t attn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
@@ -257,9 +469,6 @@ ATTN_API attn_status_t attn_fwd_f32(const float* q, const float* k, const float*
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd_f32 kernel launch");
 }
 
-namespace {
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-}
 
 ATTN_API size_t attn_decode_workspace_bytes(int B, int H, int d, int num_splits) {
     if (B < 0 || H < 0 || d <= 0 || num_splits < 1 || num_splits > 1024) return 0;

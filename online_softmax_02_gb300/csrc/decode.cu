@@ -185,47 +185,86 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
         ws_lse[slot_idx] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
 
+// 128 threads per (b, h). The partial outputs, the bulk of what the merge
+// reads, arrive as 16-byte vectors: D / 4 lanes cover one split's row of D
+// FP32 values, and the 128 threads take 128 / (D / 4) split rows at a time,
+// so every warp load is one fully used 512-byte (D = 128) or two 256-byte
+// (D = 64) contiguous segments. The rows' sums meet in shared memory.
+constexpr int kCombineThreads = 128;
+
 template <int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(kCombineThreads)
 decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int H,
                       int num_splits) {
-    extern __shared__ float sm_w[];          // num_splits weights
-    __shared__ float red[D / 32];
+    constexpr int LPR = D / 4;                       // lanes per split row (one float4 each)
+    constexpr int RPI = kCombineThreads / LPR;       // split rows per iteration
+    extern __shared__ float sm_w[];                  // num_splits weights
+    __shared__ __align__(16) float4 part[RPI][LPR];
+    __shared__ float red[kCombineThreads / 32];
     __shared__ float bcast;
     // every partial is written by the split grid, which must have completed
     // (a no-op when launched without the programmatic attribute)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long bh = static_cast<long long>(blockIdx.y) * H + blockIdx.x;
     const float* lp = ws_lse + bh * num_splits;
+    const int tid = threadIdx.x;
     // m* = max_s lse_s
     float mx = -INFINITY;
-    for (int s = threadIdx.x; s < num_splits; s += D) mx = fmaxf(mx, lp[s]);
+    for (int s = tid; s < num_splits; s += kCombineThreads) mx = fmaxf(mx, lp[s]);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = mx;
+    if (tid % 32 == 0) red[tid / 32] = mx;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         float t = -INFINITY;
-        for (int w = 0; w < D / 32; ++w) t = fmaxf(t, red[w]);
+#pragma unroll
+        for (int w = 0; w < kCombineThreads / 32; ++w) t = fmaxf(t, red[w]);
         bcast = t;
     }
     __syncthreads();
     const float M = bcast;
     const float M_ref = (M == -INFINITY) ? 0.f : M;
     // w_s = exp(lse_s - m*)
-    for (int s = threadIdx.x; s < num_splits; s += D)
+    for (int s = tid; s < num_splits; s += kCombineThreads)
         sm_w[s] = ptx::ex2((lp[s] - M_ref) * kLog2e);
     __syncthreads();
-    float W = 0.f, A = 0.f;
-    const float* op = ws_o + bh * num_splits * D + threadIdx.x;
-    for (int s = 0; s < num_splits; ++s) {
+    // sum_s w_s o_s, 16 bytes per lane per split row
+    const int r = tid / LPR, c = tid % LPR;
+    const float4* op = reinterpret_cast<const float4*>(ws_o + bh * num_splits * D) + c;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float W = 0.f;
+    for (int s = r; s < num_splits; s += RPI) {
         const float w = sm_w[s];
-        W += w;
-        A = fmaf(w, op[static_cast<long long>(s) * D], A);
+        const float4 x = op[static_cast<long long>(s) * LPR];
+        a.x = fmaf(w, x.x, a.x);
+        a.y = fmaf(w, x.y, a.y);
+        a.z = fmaf(w, x.z, a.z);
+        a.w = fmaf(w, x.w, a.w);
     }
-    o[bh * D + threadIdx.x] = __float2bfloat16_rn(W > 0.f ? A / W : 0.f);
-    if (lse != nullptr && threadIdx.x == 0) lse[bh] = (W > 0.f) ? M + logf(W) : -INFINITY;
+    part[r][c] = a;
+    if (tid < 32) {
+        for (int s = tid; s < num_splits; s += 32) W += sm_w[s];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+        if (tid == 0) bcast = W;
+    }
+    __syncthreads();
+    if (tid < LPR) {
+        float4 t = part[0][tid];
+#pragma unroll
+        for (int rr = 1; rr < RPI; ++rr) {
+            const float4 u = part[rr][tid];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        const float Wt = bcast;
+        const float inv = Wt > 0.f ? 1.f / Wt : 0.f;
+        uint2 packed;
+        packed.x = pack_bf16x2(t.x * inv, t.y * inv);
+        packed.y = pack_bf16x2(t.z * inv, t.w * inv);
+        *reinterpret_cast<uint2*>(o + bh * D + 4 * tid) = packed;
+        if (lse != nullptr && tid == 0) lse[bh] = (Wt > 0.f) ? M + logf(Wt) : -INFINITY;
+    }
 }
 
 }  // namespace
@@ -245,7 +284,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = g2;
-    cfg.blockDim = dim3(a.d == 64 ? 64 : 128);
+    cfg.blockDim = dim3(kCombineThreads);
     cfg.dynamicSmemBytes = smem2;
     cfg.stream = stream;
     cfg.attrs = attr;

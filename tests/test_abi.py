@@ -174,3 +174,43 @@ def test_exp2_soft_argument_errors(lib, kw, code):
     a = dict(x=FAKE, y=FAKE, n=8)
     a.update(kw)
     assert lib.attn_exp2_soft(a["x"], a["y"], a["n"], None) == code
+
+
+def test_host_workspace_size(lib):
+    # 2*3 heads in groups of 2 (3 groups), 2 slots: per slot q, k, v, o BF16
+    # and lse FP32 for 2 heads, each region padded to 256 bytes; then the
+    # per-head and per-batch key lengths
+    B, H, Nq, Nk, d = 2, 3, 10, 20, 64
+    a256 = lambda x: (x + 255) // 256 * 256
+    slot = 2 * a256(2 * Nq * d * 2) + 2 * a256(2 * Nk * d * 2) + a256(2 * Nq * 4)
+    assert lib.attn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, 3, 2) == 2 * slot + a256(6 * 4 + 2 * 4)
+    # more slots than groups: only as many buffer sets as groups
+    assert lib.attn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, 3, 8) == 3 * slot + 256
+    for bad in ((B, H, Nq, Nk, 96, 3, 2), (B, H, Nq, Nk, d, 0, 2), (B, H, Nq, Nk, d, 3, 0),
+                (B, H, Nq, Nk, d, 3, 9), (-1, H, Nq, Nk, d, 3, 2)):
+        assert lib.attn_fwd_host_workspace_bytes(*bad) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), 2),
+    (dict(groups=0), 1),
+    (dict(slots=0), 1),
+    (dict(slots=9), 1),
+    (dict(ws=None), 1),
+    (dict(ws_bytes=100), 1),
+    (dict(ws=FAKE + 16), 1),
+    (dict(mask_kind=4, seqlens=None), 1),
+    (dict(q=FAKE + 1), 1),
+    (dict(lse=FAKE + 2), 1),
+    (dict(scale=-1.0), 1),
+])
+def test_fwd_host_argument_errors(lib, kw, code):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, H=2, Nq=16, Nk=16, d=128,
+             scale=0.125, mask_kind=0, window=0, seqlens=None, groups=2, slots=2, ws=FAKE,
+             ws_bytes=1 << 24)
+    a.update(kw)
+    st = lib.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+                           a["Nk"], a["d"], a["scale"], a["mask_kind"], a["window"],
+                           a["seqlens"], a["groups"], a["slots"], a["ws"], a["ws_bytes"], None)
+    assert st == code
+    assert lib.attn_last_error() != b""

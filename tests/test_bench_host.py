@@ -38,6 +38,17 @@ def test_visible_pairs_matches_brute_force(mask_kind, window, seqlens):
                for b in range(3)) * 2
     assert got == want
     assert bench.flops(w, seqlens) == 4.0 * 8 * want
+    # the per-row count the CPU baselines use sums to the same total
+    rows = np.arange(3 * 2 * 33)
+    per_row = bench.row_visible_keys(w, rows, seqlens)
+    assert int(per_row.sum()) == want
+    for r in (0, 5, 32, 33, 100, 197):
+        b, i = r // (2 * 33), r % 33
+        L = 37 if seqlens is None else seqlens[b]
+        assert per_row[r] == sum(
+            1 for j in range(37) if j < L
+            and (not mask_kind & (W.MASK_CAUSAL | W.MASK_WINDOW) or j <= i)
+            and (not mask_kind & W.MASK_WINDOW or j > i - window))
 
 
 def test_workload_flop_counts():
