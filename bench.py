@@ -341,6 +341,8 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
         return run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result)
     # ---------------- causal workload
     wc = W.CAUSAL
+    if args.batch:
+        wc = dataclasses.replace(wc, B=args.batch, name="%s_B%d" % (wc.name, args.batch))
     xc = W.generate(wc)
     qc, kc, vc = (xc[n].to(dev) for n in ("q", "k", "v"))
     oc = torch.empty_like(qc)
@@ -374,6 +376,8 @@ def run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result):
     if args.only not in ("all", "masked"):
         return run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result)
     wm = W.MASKED
+    if args.batch:
+        wm = dataclasses.replace(wm, B=args.batch, name="%s_B%d" % (wm.name, args.batch))
     xm = W.generate(wm)
     qm, km, vm = (xm[n].to(dev) for n in ("q", "k", "v"))
     sl = xm["seqlens_k"].to(dev)
@@ -757,6 +761,8 @@ def main():
                                        "decode", "softmax"], default="all")
     ap.add_argument("--heads", type=int, default=0, help="override H of the prefill workload")
     ap.add_argument("--decode-nk", type=int, default=0, help="override Nk of the decode workload")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override B of the causal and masked workloads")
     ap.add_argument("--softmax-rows", type=int, default=0,
                     help="override the row count of the softmax workload")
     args = ap.parse_args()

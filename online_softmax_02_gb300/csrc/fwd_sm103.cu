@@ -77,6 +77,7 @@
 //   * Every mbarrier wait is bounded; on expiry the CTA records the site in
 //     the device error word, all roles stop, in-flight copies and MMAs are
 //     drained, tensor memory is freed and the kernel returns.
+#include <algorithm>
 #include <climits>
 #include "common.cuh"
 
@@ -199,7 +200,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  float* __restrict__ lse, int H, int Nq, int Nk, float scale_log2, float o_mul,
                  int mask_kind, int window, const int* __restrict__ seqlens_k,
-                 unsigned int* __restrict__ err, int reverse_order) {
+                 unsigned int* __restrict__ err, int group_heads) {
     using C = Cfg<D, F8>;
     constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
     extern __shared__ uint8_t smem_raw[];
@@ -211,17 +212,26 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // Unmasked: the pairs of one head are adjacent (they share K and V in
-    // L2). Causal or windowed: the longest pairs of every head come first,
-    // so the last wave holds the shortest CTAs instead of one head's
-    // longest ones.
+    // Unmasked (group_heads == 0): the pairs of one head are adjacent (they
+    // share K and V in L2). Causal or windowed: the heads are taken in groups
+    // of group_heads, and within a group the longest pairs of every head
+    // come first, so the last wave holds the shortest CTAs instead of one
+    // head's longest ones, while the K and V of the heads in flight (one
+    // group, two at a group boundary) stay within L2 (all heads at once
+    // re-read K and V from device memory about five times on the causal
+    // workload).
     int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    if (reverse_order) {
+    if (group_heads > 0) {
         const int nbh = gridDim.y * gridDim.z;
-        const long long lin = blockIdx.x + static_cast<long long>(gridDim.x) *
+        const int pairs = gridDim.x;
+        const long long lin = blockIdx.x + static_cast<long long>(pairs) *
                                                (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
-        pair = static_cast<int>(gridDim.x - 1 - lin / nbh);
-        const int bhl = static_cast<int>(lin % nbh);
+        const long long per_group = static_cast<long long>(group_heads) * pairs;
+        const int g = static_cast<int>(lin / per_group);
+        const int idx = static_cast<int>(lin - g * per_group);
+        const int gh = min(group_heads, nbh - g * group_heads);   // heads in this group
+        pair = pairs - 1 - idx / gh;
+        const int bhl = g * group_heads + idx % gh;
         h = bhl % H;
         b = bhl / H;
     }
@@ -768,10 +778,18 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
     }
     const int pairs = (a.Nq + BM * NT - 1) / (BM * NT);
     dim3 grid(pairs, a.H, a.B);
-    const int reverse = (a.mask_kind & (kMaskCausal | kMaskWindow)) ? 1 : 0;
+    // Causal or windowed: longest pairs first within groups of heads whose
+    // K and V together take about 32 MiB (a quarter of L2).
+    int group_heads = 0;
+    if (a.mask_kind & (kMaskCausal | kMaskWindow)) {
+        const long long nbh = static_cast<long long>(a.B) * a.H;
+        const long long kv_head = 2LL * a.Nk * a.d * C::kElem;
+        const long long g = std::max(1LL, (32LL << 20) / std::max(kv_head, 1LL));
+        group_heads = static_cast<int>(std::min(g, nbh));
+    }
     fwd_sm103_kernel<D, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(
         tq, tk, tv, to, a.lse, a.H, a.Nq, a.Nk, scale_log2, o_mul,
-        a.mask_kind, a.window, a.seqlens_k, a.err, reverse);
+        a.mask_kind, a.window, a.seqlens_k, a.err, group_heads);
     return cudaGetLastError();
 }
 
