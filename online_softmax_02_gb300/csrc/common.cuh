@@ -30,6 +30,8 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 // (returns false) when `*abort_flag` is set by another role of the CTA, or
 // after `limit` cycles, in which case it records the site in the error word
 // and raises the CTA's abort flag so that the other roles stop too.
+// `abort_flag` may be NULL (the drain waits, which run after the roles have
+// stopped): then only the limit ends the wait.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, unsigned int* err,
                                              uint32_t site, long long limit = kWaitLimitCycles) {
@@ -37,9 +39,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     const long long t0 = clock64();
     while (true) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
+        if (abort_flag != nullptr && *abort_flag) return false;
         if (clock64() - t0 > limit) {
-            *abort_flag = 1;
+            if (abort_flag != nullptr) *abort_flag = 1;
             atomicCAS(err, 0u, (site << 8) | 1u);
             return false;
         }
