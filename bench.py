@@ -51,20 +51,32 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the source file of the kernel and its
 # SHA-256 at capture time; reported as null when the source has changed.
+FWD_SHA = "4178639fb660ab722899a927c57ff1276818cc2c50efe1db6560ca42867619f6"
+DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
+BWD_SHA = "dd91f3180f1e946c45efeb6fdb38f78c27338bffd1fb4cbadddc259339dc7c37"
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
     # launch at the full bench workload, 1-pass ncu capture; valid while the
     # kernel source is unchanged.
-    "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": "195b3626a3f55a77002b8c722fe2ec8e77fecb64aa32e0ae5d772e323a6faa6b",
-                 "bytes_per_launch": 402933504 + 115678464,
+    "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
+                 "bytes_per_launch": 403099136 + 116022272,
                  "workload": "prefill_B1_H64_N8192_d128_bf16"},
-    "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": "195b3626a3f55a77002b8c722fe2ec8e77fecb64aa32e0ae5d772e323a6faa6b",
-                 "bytes_per_launch": 201414144 + 104146432,
+    "fwd_bf16_causal": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
+                        "bytes_per_launch": 403559424 + 115297792,
+                        "workload": "causal_B2_H32_N8192_d128_bf16"},
+    "fwd_bf16_masked": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
+                        "bytes_per_launch": 243448832 + 109369088,
+                        "workload": "masked_B8_H16_N4096_d128_bf16_window1024_padded"},
+    "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
+                 "bytes_per_launch": 201975808 + 104190976,
                  "workload": "prefill_B1_H64_N8192_d128_e4m3"},
-    "decode": {"file": "decode.cu",
-               "sha256": "1e8433d0c2c945f4dff3e0d753f60c24f853a2730e97cfd0e826e9ce628a67d1",
-               "bytes_per_launch": 2147533056 + 3133184,
-               "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split kernel)"},
+    "decode": {"file": "decode.cu", "sha256": DECODE_SHA,
+               "bytes_per_launch": 2147542528 + 3053312 + 1072640,
+               "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split and combine kernels)"},
+    "backward": {"file": "bwd_sm103.cu", "sha256": BWD_SHA,
+                 "bytes_per_launch": (270548992 + 5424640) + (541174528 + 237196544) +
+                                     (541544192 + 115900416),
+                 "workload": "prefill_B1_H64_N8192_d128_bf16 backward (prep, dK/dV and dQ kernels)"},
     "softmax": {"file": "softmax.cu",
                 "sha256": "9a40d74a21d385c58919240ac5c54e555e31ccc3e2bd568868bc0f51f562068d",
                 "bytes_per_launch": 537604096 + 475967488,
@@ -246,6 +258,8 @@ def whole_job_rate(units_per_step, world, steps, total_ms):
 def run_ours(args, rank, world, dist_on):
     import online_softmax_02_gb300 as attn
     attn.load()
+    # another build for the forward sections (--lib), or the default library
+    args.fwd_lib = attn.open_build(os.path.abspath(args.lib)) if args.lib else None
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
@@ -264,11 +278,12 @@ def run_ours(args, rank, world, dist_on):
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
 
     def step():
-        attn.attn_fwd(q, k, v, o=o, lse=lse, mask_kind=w.mask_kind, stream=stream)
+        attn.attn_fwd(q, k, v, o=o, lse=lse, mask_kind=w.mask_kind, stream=stream,
+                      lib=args.fwd_lib)
 
     with ClockSampler(gpu_uuid(dev)) as clk:
         total_ms, per = time_loop(step, args.steps, args.warmup, stream, dist_on)
-    attn.attn_check_device_error(stream)
+    attn.attn_check_device_error(stream, lib=args.fwd_lib)
     total_ms = max_over_ranks(total_ms, dist_on)
     fl = flops(w)
     ms_step = total_ms / args.steps
@@ -322,7 +337,8 @@ def run_ours(args, rank, world, dist_on):
         "dtype": "bf16", "data": "synthetic (seeded N(0,1), rounded to BF16)",
         "config": dict(w.describe(), **{"parallelism": "replicas" if world > 1 else "single",
                                         "l2": "inputs larger than L2 (384 MiB); no flush",
-                                        "flop_count": "4*d per visible (query, key) pair"}),
+                                        "flop_count": "4*d per visible (query, key) pair"},
+                       **({"library": args.lib} if args.lib else {})),
         "gpu_launches": args.steps,
         "e2e": e2e,
         "roofline": roofline,
@@ -349,10 +365,11 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
     lc = torch.empty(qc.shape[:3], dtype=torch.float32, device=dev)
 
     def step_c():
-        attn.attn_fwd(qc, kc, vc, o=oc, lse=lc, mask_kind=wc.mask_kind, stream=stream)
+        attn.attn_fwd(qc, kc, vc, o=oc, lse=lc, mask_kind=wc.mask_kind, stream=stream,
+                      lib=args.fwd_lib)
 
     c_total, c_per = time_loop(step_c, args.steps, args.warmup, stream, dist_on)
-    attn.attn_check_device_error(stream)
+    attn.attn_check_device_error(stream, lib=args.fwd_lib)
     c_total = max_over_ranks(c_total, dist_on)
     flc = flops(wc)
     causal = {"config": wc.describe(), "ms_per_step": round(c_total / args.steps, 4),
@@ -362,7 +379,7 @@ def run_sections(args, rank, world, dist_on, dev, stream, peaks, result):
               "dense_equivalent_tflops": round(4.0 * wc.d * wc.B * wc.H * wc.Nq * wc.Nk * world *
                                                args.steps / (c_total * 1e-3) / 1e12, 2),
               "roofline": tensor_roofline(flc, c_per, peaks, "fwd_bf16_causal",
-                                          "fwd_sm103_kernel<128> (causal)")}
+                                          "fwd_sm103_kernel<128> (causal)", wc.B / W.CAUSAL.B)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         causal["cpu_baseline"] = cpu_baseline(wc, xc, oc, lc, args, args.cpu_seconds / 2)
     del qc, kc, vc, oc, lc, xc
@@ -386,10 +403,10 @@ def run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result):
 
     def step_m():
         attn.attn_fwd(qm, km, vm, o=om, lse=lm, mask_kind=wm.mask_kind, window=wm.window,
-                      seqlens_k=sl, stream=stream)
+                      seqlens_k=sl, stream=stream, lib=args.fwd_lib)
 
     m_total, m_per = time_loop(step_m, args.steps, args.warmup, stream, dist_on)
-    attn.attn_check_device_error(stream)
+    attn.attn_check_device_error(stream, lib=args.fwd_lib)
     m_total = max_over_ranks(m_total, dist_on)
     flm = flops(wm, xm["seqlens_k"].numpy())
     result["masked"] = {
@@ -397,7 +414,8 @@ def run_masked_section(args, rank, world, dist_on, dev, stream, peaks, result):
         "value": round(flm * world * args.steps / (m_total * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
         "flop_count": "visible pairs only (window and padding)", "gpu_launches_per_step": 1,
         "roofline": tensor_roofline(flm, m_per, peaks, "fwd_bf16_masked",
-                                    "fwd_sm103_kernel<128> (window + padding)")}
+                                    "fwd_sm103_kernel<128> (window + padding)",
+                                    wm.B / W.MASKED.B)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["masked"]["cpu_baseline"] = cpu_baseline(wm, xm, om, lm, args,
                                                         args.cpu_seconds / 2)
@@ -480,7 +498,8 @@ def run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": None, "note": "time of the three launches per step"}}
+                     "traffic": traffic_for("backward", w.H / W.PREFILL.H),
+                     "note": "time and DRAM traffic of the three launches per step"}}
     del q, k, v, do, o, lse, dq, dk, dv, ws, x
     return run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result)
 
@@ -615,12 +634,12 @@ def naive_attention_context(args, dev, stream, peaks):
     return out
 
 
-def tensor_roofline(fl, per_launch_ms, peaks, traffic_key, kernel):
+def tensor_roofline(fl, per_launch_ms, peaks, traffic_key, kernel, units_scale=1.0):
     """Roofline of a forward launch against the measured dense BF16 burst."""
     achieved = fl / (statistics.mean(per_launch_ms) * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-            "traffic": traffic_for(traffic_key), "kernel": kernel,
+            "traffic": traffic_for(traffic_key, units_scale), "kernel": kernel,
             "algorithmic_flops_per_launch": fl}
 
 
@@ -765,6 +784,9 @@ def main():
                     help="override B of the causal and masked workloads")
     ap.add_argument("--softmax-rows", type=int, default=0,
                     help="override the row count of the softmax workload")
+    ap.add_argument("--lib", default=None,
+                    help="another build of libattn.so for the forward sections (one made by "
+                         "python -m online_softmax_02_gb300.build -D ... --out PATH)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

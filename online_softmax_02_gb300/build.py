@@ -77,5 +77,19 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str |
 
 
 if __name__ == "__main__":
-    import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    # python -m online_softmax_02_gb300.build [--force] [-v] [-D NAME=VALUE ... --out PATH]
+    # A build with -D options goes to its own library (--out) and build folder.
+    import argparse
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("-v", dest="verbose", action="store_true")
+    ap.add_argument("-D", dest="defines", action="append", default=[],
+                    help="compile-time option, e.g. -D ATTN_FWD_PAIR=1")
+    ap.add_argument("--out", default=None, help="library path of a build with -D options")
+    args = ap.parse_args()
+    if args.defines and not args.out:
+        ap.error("a build with -D options needs --out (the default library stays untouched)")
+    out = os.path.abspath(args.out) if args.out else None
+    bdir = None if out is None else os.path.join(os.path.dirname(out), "_objs")
+    print(build(force=args.force, verbose=args.verbose,
+                extra_flags=tuple("-D" + d for d in args.defines), out=out, build_dir=bdir))

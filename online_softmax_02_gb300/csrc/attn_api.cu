@@ -19,13 +19,25 @@
 namespace attn {
 
 cudaError_t launch_fwd_sm103_maps(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, const CUtensorMap& to,
+                                  const CUtensorMap& tv, const CUtensorMap& to, bool pair,
                                   cudaStream_t stream);
 cudaError_t launch_fwd_fp8_maps(const FwdArgs& a, float descale_q, float descale_k,
                                 float descale_v, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream);
 
 namespace {
+
+// 1: the BF16 forward at d = 128 runs on CTA pairs (cta_group::2: each K/V
+// block is split between two SMs and every MMA spans both). 0 (default): the
+// one-CTA kernel, which d = 64 and the E4M3 forward always use. The pair form
+// measured slower on GB300 (prefill B1 H64 8192^2: 1.65 against 1.34 ms;
+// causal 0.92 against 0.70): the forward's pace is set by the softmax -> P
+// -> MMA hand-off, and in a pair each hand-off crosses to the other SM and
+// waits for the slower of two softmaxes.
+#ifndef ATTN_FWD_PAIR
+#define ATTN_FWD_PAIR 0
+#endif
+constexpr bool kFwdPair = ATTN_FWD_PAIR != 0;
 
 __device__ unsigned int g_err_word = 0;   // see WaitSite in common.cuh
 
@@ -180,12 +192,14 @@ attn_status_t fwd_bf16_launch(const void* q, const void* k, const void* v, void*
     if ((st = err_word(&err)) != ATTN_OK) return st;
     CUtensorMap tq, tk, tv, to;
     const long long bh = static_cast<long long>(B) * H;
+    // d = 128 runs on CTA pairs, each CTA loading 64 keys of every K block
+    const bool pair = kFwdPair && d == 128;
     if ((st = encode_bf16_3d(&tq, q, d, Nq, bh)) != ATTN_OK) return st;
-    if ((st = encode_bf16_3d(&tk, k, d, Nk, bh)) != ATTN_OK) return st;
+    if ((st = encode_3d(&tk, k, d, Nk, bh, false, pair ? 64 : 128)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tv, v, d, Nk, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&to, o, d, Nq, bh)) != ATTN_OK) return st;   // the epilogue's stores
     FwdArgs a{q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, seqlens_k, err};
-    cudaError_t e = launch_fwd_sm103_maps(a, tq, tk, tv, to, s);
+    cudaError_t e = launch_fwd_sm103_maps(a, tq, tk, tv, to, pair, s);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd kernel launch");
 }
 

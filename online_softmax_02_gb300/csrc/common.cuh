@@ -31,14 +31,19 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 // after `limit` cycles, in which case it records the site in the error word
 // and raises the CTA's abort flag so that the other roles stop too.
 // `abort_flag` may be NULL (the drain waits, which run after the roles have
-// stopped): then only the limit ends the wait.
+// stopped): then only the limit ends the wait. kCluster: acquire at cluster
+// scope (barriers that the other CTA of a pair signals).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, unsigned int* err,
                                              uint32_t site, long long limit = kWaitLimitCycles) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto test = [&]() {
+        return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (test()) return true;
     const long long t0 = clock64();
     while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (test()) return true;
         if (abort_flag != nullptr && *abort_flag) return false;
         if (clock64() - t0 > limit) {
             if (abort_flag != nullptr) *abort_flag = 1;

@@ -77,6 +77,20 @@
 //   * Every mbarrier wait is bounded; on expiry the CTA records the site in
 //     the device error word, all roles stop, in-flight copies and MMAs are
 //     drained, tensor memory is freed and the kernel returns.
+//   * CTA-pair form (PAIR, BF16 at d = 128; a compile-time choice of the
+//     library, off by default). Clusters of two CTAs own four tiles; tile t
+//     of the pair is one M = 256 MMA (tcgen05 cta_group::2) over 128 rows of
+//     each CTA. Each CTA loads half of every K block (64 keys) and half of
+//     every V block (64 head dims), so the tensor cores read half as much B
+//     operand from each SM's shared memory. The first CTA issues every MMA;
+//     its commits arrive on both CTAs' barriers (multicast), both CTAs'
+//     copies count on its step barriers (cta_group::2 TMA), and the second
+//     CTA's softmax warps hand P over by remote arrivals on its P barriers.
+//     Same arithmetic as the one-CTA kernel (identical results), but slower
+//     on GB300 (prefill B1 H64 8192^2: 1.49-1.65 against 1.29-1.34 ms; tensor
+//     pipe 57 % against 74 % active): the forward's pace is set by the
+//     softmax -> P -> MMA hand-off, and in a pair every hand-off crosses to
+//     the other SM and waits for the slower of two softmaxes.
 #include <algorithm>
 #include <climits>
 #include "common.cuh"
@@ -120,19 +134,26 @@ __host__ __device__ constexpr bool soft_pair(int idx) {
 }
 
 // F8 = false: BF16 Q, K, V (kind::f16, K = 16 per MMA); F8 = true: E4M3
-// Q, K, V (kind::f8f6f4, K = 32 per MMA), d = 128 only.
-template <int D, bool F8>
+// Q, K, V (kind::f8f6f4, K = 32 per MMA), d = 128 only. PAIR: the CTA-pair
+// form (BF16, d = 128): each MMA spans the tensor cores of two SMs (M = 256,
+// 128 query rows from each CTA) and each CTA holds half of every K block
+// (64 keys) and half of every V block (64 head dims).
+template <int D, bool F8, bool PAIR = false>
 struct Cfg {
+    static_assert(!PAIR || (D == 128 && !F8), "the CTA-pair form is BF16 with d = 128");
     static constexpr int kElem = F8 ? 1 : 2;                   // bytes per element
     static_assert((D * kElem) % 128 == 0, "head dim must fill 128-byte swizzle rows");
     // K/V ring depths: K is consumed one MMA step ahead of V, so it gets the
     // deeper ring (BF16, d = 128: Q 64 KiB + K 3 x 32 KiB + V 2 x 32 KiB =
     // 224 KiB; E4M3: Q 32 KiB + K 6 x 16 KiB + V 5 x 16 KiB = 208 KiB, 1 %
-    // faster than 4 + 4 on the E4M3 prefill). The V ring must be the
-    // shallower one: step barriers (one per K slot) also carry V.
-    static constexpr int kStagesK = F8 ? 6 : (D == 64) ? 5 : 3;
-    static constexpr int kStagesV = F8 ? 5 : (D == 64) ? 4 : 2;
+    // faster than 4 + 4 on the E4M3 prefill; pair: Q 64 KiB + K 5 x 16 KiB +
+    // V 4 x 16 KiB = 208 KiB). The V ring must be the shallower one: step
+    // barriers (one per K slot) also carry V.
+    static constexpr int kStagesK = PAIR ? 5 : F8 ? 6 : (D == 64) ? 5 : 3;
+    static constexpr int kStagesV = PAIR ? 4 : F8 ? 5 : (D == 64) ? 4 : 2;
     static_assert(kStagesV < kStagesK, "a V load may not reach a step barrier's next phase");
+    static constexpr int kCtas = PAIR ? 2 : 1;                 // CTAs sharing one MMA
+    static constexpr int kMmaM = BM * kCtas;                   // query rows per MMA
     static constexpr uint32_t kRowBytes = 128;                 // one swizzle atom row
     static constexpr int kChunkElems = 128 / kElem;            // head dims per atom row
     static constexpr int kChunks = D * kElem / 128;
@@ -141,14 +162,18 @@ struct Cfg {
     static constexpr int kPVSteps = BN / kPVKeys;               // P V MMAs per block
     static constexpr uint32_t kPHalfCols = (BN / 2) * kElem / 4;   // TMEM columns of half of P
     static constexpr uint32_t kQTileBytes = BM * D * kElem;
-    static constexpr uint32_t kKVBytes = BN * D * kElem;
+    static constexpr uint32_t kKVBytes = BN * D * kElem;       // a whole K or V block
+    static constexpr uint32_t kSlotBytes = kKVBytes / kCtas;   // this CTA's share of one
+    static constexpr int kKRows = BN / kCtas;                  // keys of a K block held here
     static constexpr uint32_t kQChunkBytes = BM * kRowBytes;   // one atom column of a Q tile
-    static constexpr uint32_t kKVChunkBytes = BN * kRowBytes;  // one atom column of a K/V block
+    static constexpr uint32_t kKChunkBytes = kKRows * kRowBytes;   // one atom column of a K slot
+    static constexpr uint32_t kVChunkBytes = BN * kRowBytes;   // one atom column of a V slot
     static constexpr uint32_t kQOff = 0;
     static constexpr uint32_t kKOff = kQOff + NT * kQTileBytes;
-    static constexpr uint32_t kVOff = kKOff + kStagesK * kKVBytes;
-    static constexpr uint32_t kBarOff = kVOff + kStagesV * kKVBytes;
-    // barrier indices
+    static constexpr uint32_t kVOff = kKOff + kStagesK * kSlotBytes;
+    static constexpr uint32_t kBarOff = kVOff + kStagesV * kSlotBytes;
+    // barrier indices (pair: QFull, Step and PFull are used in the first
+    // CTA only, where the MMAs are issued; the others in both)
     static constexpr int bQFull = 0;
     static constexpr int bStep = 1;                    // [NSK]: step s has K_s and V_{s-1}
     static constexpr int bKEmpty = bStep + kStagesK;
@@ -168,11 +193,11 @@ struct Cfg {
 
 struct Range { int lo, hi; };   // key blocks [lo, hi)
 
-// Key blocks that some row of the tile [row_first, row_first + BM) can see.
-__device__ __forceinline__ Range tile_range(int row_first, int Nq, int Lk, bool causal,
+// Key blocks that some row of [row_first, row_first + rows) can see.
+__device__ __forceinline__ Range tile_range(int row_first, int rows, int Nq, int Lk, bool causal,
                                             bool windowed, int window) {
     if (row_first >= Nq) return {0, 0};
-    const int row_last = min(row_first + BM, Nq) - 1;
+    const int row_last = min(row_first + rows, Nq) - 1;
     int key_hi = Lk;
     if (causal) key_hi = min(key_hi, row_last + 1);
     const int key_lo = windowed ? max(0, row_first - window + 1) : 0;
@@ -193,15 +218,16 @@ __device__ __forceinline__ bool block_needs_mask(int kb, int row_first, int Lk, 
 
 // 352 threads, one CTA per SM. The register file is split by sub-partition
 // (16,384 each) and three of the eleven warps share one, so a thread gets at
-// most 168 registers.
-template <int D, bool F8>
+// most 168 registers. PAIR: launched in clusters of two CTAs (x), which
+// together own four query tiles; CTA 0 issues every MMA of the pair.
+template <int D, bool F8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  float* __restrict__ lse, int H, int Nq, int Nk, float scale_log2, float o_mul,
                  int mask_kind, int window, const int* __restrict__ seqlens_k,
                  unsigned int* __restrict__ err, int group_heads) {
-    using C = Cfg<D, F8>;
+    using C = Cfg<D, F8, PAIR>;
     constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -212,49 +238,86 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // Unmasked (group_heads == 0): the pairs of one head are adjacent (they
+    // rank in the pair (0 issues the MMAs); the pair's barriers that collect
+    // both CTAs' copies and P hand-offs live in CTA 0, addressed through
+    // the cluster window.
+    const int rank = PAIR ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+    const bool issuer_cta = rank == 0;
+    auto lead_bar = [&](int i) -> uint32_t {
+        if constexpr (PAIR) return ptx::mapa_shared(bar(i), 0);
+        else return bar(i);
+    };
+    // Unmasked (group_heads == 0): the units of one head are adjacent (they
     // share K and V in L2). Causal or windowed: the heads are taken in groups
-    // of group_heads, and within a group the longest pairs of every head
+    // of group_heads, and within a group the longest units of every head
     // come first, so the last wave holds the shortest CTAs instead of one
     // head's longest ones, while the K and V of the heads in flight (one
     // group, two at a group boundary) stay within L2 (all heads at once
     // re-read K and V from device memory about five times on the causal
-    // workload).
-    int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // workload). A unit is the NT tiles of one CTA, or of a CTA pair.
+    const int units = gridDim.x / C::kCtas;
+    int unit = blockIdx.x / C::kCtas, h = blockIdx.y, b = blockIdx.z;
     if (group_heads > 0) {
         const int nbh = gridDim.y * gridDim.z;
-        const int pairs = gridDim.x;
-        const long long lin = blockIdx.x + static_cast<long long>(pairs) *
-                                               (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
-        const long long per_group = static_cast<long long>(group_heads) * pairs;
+        const long long lin = unit + static_cast<long long>(units) *
+                                         (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+        const long long per_group = static_cast<long long>(group_heads) * units;
         const int g = static_cast<int>(lin / per_group);
         const int idx = static_cast<int>(lin - g * per_group);
         const int gh = min(group_heads, nbh - g * group_heads);   // heads in this group
-        pair = pairs - 1 - idx / gh;
+        unit = units - 1 - idx / gh;
         const int bhl = g * group_heads + idx % gh;
         h = bhl % H;
         b = bhl / H;
     }
     const int bh = b * H + h;
-    const int q0 = pair * (BM * NT);
+    // Tile t of the unit covers rows [q0 + t * kMmaM, + kMmaM); this CTA's
+    // share of it starts at own_row(t).
+    const int q0 = unit * (C::kMmaM * NT);
+    auto own_row = [&](int t) { return q0 + t * C::kMmaM + rank * BM; };
 
     int Lk = Nk;
     if (mask_kind & kMaskPadding) Lk = min(max(seqlens_k[b], 0), Nk);
     const bool causal = (mask_kind & (kMaskCausal | kMaskWindow)) != 0;
     const bool windowed = (mask_kind & kMaskWindow) != 0;
 
+    // Key-block ranges of the MMA tiles (pair: the union over both CTAs'
+    // rows, identical in both CTAs)
     Range R[NT];
     int lo = INT_MAX, hi = 0;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        R[t] = tile_range(q0 + t * BM, Nq, Lk, causal, windowed, window);
+        R[t] = tile_range(q0 + t * C::kMmaM, C::kMmaM, Nq, Lk, causal, windowed, window);
         if (R[t].lo < R[t].hi) { lo = min(lo, R[t].lo); hi = max(hi, R[t].hi); }
     }
     if (hi == 0) lo = 0;
+    int nq = 0;           // tiles that see some key (their Q is loaded)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) nq += (R[t].lo < R[t].hi) ? 1 : 0;
+    // This CTA's Q tiles, loaded into its own shared memory; completion is
+    // counted on the issuing CTA's barrier. Only tiles that see some key: an
+    // empty tile's buffer is written by its epilogue straight away and must
+    // not receive a late Q.
+    auto load_q = [&]() {
+        ptx::prefetch_tmap(&tm_q);
+        for (int t = 0; t < NT; ++t) {
+            if (R[t].lo >= R[t].hi) continue;
+            for (int c = 0; c < C::kChunks; ++c) {
+                const uint32_t dst = sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes;
+                if constexpr (PAIR)
+                    ptx::tma_load_3d_pair(dst, &tm_q, lead_bar(C::bQFull), c * C::kChunkElems,
+                                          own_row(t), bh);
+                else
+                    ptx::tma_load_3d(dst, &tm_q, bar(C::bQFull), c * C::kChunkElems, own_row(t), bh);
+            }
+        }
+    };
 
     // The Q tiles are the first thing the CTA needs and the longest load it
     // waits for: the thread that sets up the barriers starts them before the
-    // tensor-memory allocation and the block-wide barrier.
+    // tensor-memory allocation and the block-wide barrier (pair: the second
+    // CTA's, which count on the first CTA's barrier, after the cluster
+    // barrier that publishes its initialisation).
     if (warp == kProducerWarp && lane == 0) {
         ptx::mbar_init(bar(C::bQFull), 1);
         for (int s = 0; s < NSK; ++s) {
@@ -264,34 +327,34 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int s = 0; s < NSV; ++s) ptx::mbar_init(bar(C::bVEmpty + s), 1);
         for (int t = 0; t < NT; ++t) {
             ptx::mbar_init(bar(C::bSFull + t), 1);
-            ptx::mbar_init(bar(C::bPFull + t), 4);           // one arrival per softmax warp
+            ptx::mbar_init(bar(C::bPFull + t), 4 * C::kCtas);   // one arrival per softmax warp
             ptx::mbar_init(bar(C::bODone + t), 1);
         }
         ptx::mbar_init(bar(C::bDrain), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
-        if (lo < hi) {
-            // Only tiles that see some key: an empty tile's buffer is written
-            // by its epilogue straight away and must not receive a late Q.
-            int nq = 0;
-#pragma unroll
-            for (int t = 0; t < NT; ++t) nq += (R[t].lo < R[t].hi) ? 1 : 0;
-            ptx::prefetch_tmap(&tm_q);
-            ptx::mbar_arrive_expect_tx(bar(C::bQFull), nq * C::kQTileBytes);
-            for (int t = 0; t < NT; ++t) {
-                if (R[t].lo >= R[t].hi) continue;
-                for (int c = 0; c < C::kChunks; ++c)
-                    ptx::tma_load_3d(sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes,
-                                     &tm_q, bar(C::bQFull), c * C::kChunkElems, q0 + t * BM, bh);
-            }
+        if (lo < hi && issuer_cta) {
+            ptx::mbar_arrive_expect_tx(bar(C::bQFull), nq * C::kCtas * C::kQTileBytes);
+            load_q();
         }
     }
     if (warp == kMmaWarp) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), kTmemCols);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) {
+        ptx::cluster_arrive_release();
+        ptx::cluster_wait_acquire();
+        if (warp == kProducerWarp && lane == 0 && lo < hi && !issuer_cta) load_q();
+    } else {
+        __syncthreads();
+    }
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -329,13 +392,32 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                                   err, is_k ? kSiteKEmpty : kSiteVEmpty);
                     if (!__all_sync(0xffffffffu, got)) break;
                     if (leader) {
-                        ptx::mbar_arrive_expect_tx(sb, C::kKVBytes);
-                        for (int c = 0; c < C::kChunks; ++c)
-                            ptx::tma_load_3d(ring + st * C::kKVBytes + c * C::kKVChunkBytes, map, sb,
-                                             c * C::kChunkElems, (lo + b) * BN, bh);
+                        // The issuing CTA's producer expects the whole block
+                        // (pair: both CTAs' halves, which count on its barrier).
+                        if (issuer_cta) ptx::mbar_arrive_expect_tx(sb, C::kKVBytes);
+                        const uint32_t dst = ring + st * C::kSlotBytes;
+                        if constexpr (PAIR) {
+                            // K: keys [64 rank, + 64) of the block, every head
+                            // dim; V: every key, head dims [64 rank, + 64).
+                            const uint32_t lsb = lead_bar(C::bStep + i % NSK);
+                            if (is_k) {
+                                for (int c = 0; c < C::kChunks; ++c)
+                                    ptx::tma_load_3d_pair(dst + c * C::kKChunkBytes, map, lsb,
+                                                          c * C::kChunkElems,
+                                                          (lo + b) * BN + rank * C::kKRows, bh);
+                            } else {
+                                ptx::tma_load_3d_pair(dst, map, lsb, rank * C::kChunkElems,
+                                                      (lo + b) * BN, bh);
+                            }
+                        } else {
+                            const uint32_t chunk = is_k ? C::kKChunkBytes : C::kVChunkBytes;
+                            for (int c = 0; c < C::kChunks; ++c)
+                                ptx::tma_load_3d(dst + c * chunk, map, sb, c * C::kChunkElems,
+                                                 (lo + b) * BN, bh);
+                        }
                     }
                     issued = b + 1;
-                } else {
+                } else if (issuer_cta) {
                     // no block for this step: K at the last step; V at the
                     // first. K's last-step arrival waits like a load would,
                     // for the release of K_{n-NSK}.
@@ -351,12 +433,20 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (*abort_flag && leader) {
                 // Let the copies this warp started land before the CTA exits
                 // (bounded: a step's phase also needs the other producer).
-                if (is_k)
-                    wait_bounded(bar(C::bQFull), 0, nullptr, err, kSiteDrain, kWaitLimitCycles / 8);
-                for (int b = max(0, issued - ns); b < issued; ++b) {
-                    const int i = is_k ? b : b + 1;
-                    wait_bounded(bar(C::bStep + i % NSK), (i / NSK) & 1, nullptr, err, kSiteDrain,
-                                 kWaitLimitCycles / 8);
+                if (issuer_cta) {
+                    if (is_k)
+                        wait_bounded<PAIR>(bar(C::bQFull), 0, nullptr, err, kSiteDrain,
+                                           kWaitLimitCycles / 8);
+                    for (int b = max(0, issued - ns); b < issued; ++b) {
+                        const int i = is_k ? b : b + 1;
+                        wait_bounded<PAIR>(bar(C::bStep + i % NSK), (i / NSK) & 1, nullptr, err,
+                                           kSiteDrain, kWaitLimitCycles / 8);
+                    }
+                } else {
+                    // pair, second CTA: its copies count on the first CTA's
+                    // barriers, which it cannot wait on; give them time to land
+                    const long long t0 = clock64();
+                    while (clock64() - t0 < 200000) { }
                 }
             }
         }
@@ -364,51 +454,60 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ------------------------------------------------------- MMA issuer
         // The whole warp runs the schedule and waits; one elected lane issues
         // every tcgen05.mma / tcgen05.commit, so the loop state and the
-        // operand descriptors stay warp-uniform.
-        if (lo < hi) {
+        // operand descriptors stay warp-uniform. Pair: only the first CTA
+        // issues; its commits arrive on the barrier at the same offset in
+        // both CTAs.
+        if (lo < hi && issuer_cta) {
             const bool leader = ptx::elect_one();
-            constexpr uint32_t kIdescS =
-                F8 ? ptx::idesc_e4m3_f32(BM, BN, false) : ptx::idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t kIdescPV =
-                F8 ? ptx::idesc_e4m3_f32(BM, D, true) : ptx::idesc_bf16_f32(BM, D, true);
-            int p_seen[NT], pv_done[NT];
+            constexpr uint32_t kIdescS = F8 ? ptx::idesc_e4m3_f32(BM, BN, false)
+                                            : ptx::idesc_bf16_f32(C::kMmaM, BN, false);
+            constexpr uint32_t kIdescPV = F8 ? ptx::idesc_e4m3_f32(BM, D, true)
+                                             : ptx::idesc_bf16_f32(C::kMmaM, D, true);
+            auto commit = [&](int i) {
+                if constexpr (PAIR) ptx::mma_commit_pair(bar(i), 0x3);
+                else ptx::mma_commit(bar(i));
+            };
+            int pv_done[NT];
 #pragma unroll
-            for (int t = 0; t < NT; ++t) { p_seen[t] = 0; pv_done[t] = 0; }
-            bool ok = __all_sync(0xffffffffu,
-                                 wait_bounded(bar(C::bQFull), 0, abort_flag, err, kSiteQFull));
+            for (int t = 0; t < NT; ++t) pv_done[t] = 0;
+            bool ok = __all_sync(0xffffffffu, wait_bounded<PAIR>(bar(C::bQFull), 0, abort_flag, err,
+                                                                 kSiteQFull));
             // O_t (+)= P_t V_{s-1} (A = P_t from tensor memory) and S_t = Q_t K_s^T.
             auto issue_pv = [&](int t, int vst, bool first) {
-                const uint32_t vbase = sbase + C::kVOff + vst * C::kKVBytes;
-                const uint64_t vdesc0 = ptx::sdesc_sw128(vbase, C::kKVChunkBytes, 1024);
+                const uint32_t vbase = sbase + C::kVOff + vst * C::kSlotBytes;
+                const uint64_t vdesc0 = ptx::sdesc_sw128(vbase, C::kVChunkBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < C::kPVSteps; ++kk) {
                     const uint64_t bdesc = ptx::sdesc_add(vdesc0, kk * C::kPVKeys * C::kRowBytes);
                     const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+                    const uint32_t a_tm = tmem + C::s_col(t) + kk * 8;
                     if constexpr (F8)
-                        ptx::mma_ts_f8(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, bdesc,
-                                       kIdescPV, acc);
+                        ptx::mma_ts_f8(tmem + C::o_col(t), a_tm, bdesc, kIdescPV, acc);
+                    else if constexpr (PAIR)
+                        ptx::mma_ts_pair(tmem + C::o_col(t), a_tm, bdesc, kIdescPV, acc);
                     else
-                        ptx::mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8, bdesc,
-                                    kIdescPV, acc);
+                        ptx::mma_ts(tmem + C::o_col(t), a_tm, bdesc, kIdescPV, acc);
                 }
             };
             auto issue_s = [&](int t, int kst) {
                 const uint32_t qbase = sbase + C::kQOff + t * C::kQTileBytes;
-                const uint32_t kbase = sbase + C::kKOff + kst * C::kKVBytes;
+                const uint32_t kbase = sbase + C::kKOff + kst * C::kSlotBytes;
                 const uint64_t adesc0 = ptx::sdesc_sw128(qbase, 16, 1024);
                 const uint64_t bdesc0 = ptx::sdesc_sw128(kbase, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < C::kQKSteps; ++kk) {
                     const uint32_t koff = (kk / 4) * C::kQChunkBytes + (kk % 4) * 32;
-                    const uint32_t boff = (kk / 4) * C::kKVChunkBytes + (kk % 4) * 32;
+                    const uint32_t boff = (kk / 4) * C::kKChunkBytes + (kk % 4) * 32;
                     const uint64_t adesc = ptx::sdesc_add(adesc0, koff);
                     const uint64_t bdesc = ptx::sdesc_add(bdesc0, boff);
                     if constexpr (F8)
                         ptx::mma_ss_f8(tmem + C::s_col(t), adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
+                    else if constexpr (PAIR)
+                        ptx::mma_ss_pair(tmem + C::s_col(t), adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
                     else
                         ptx::mma_ss(tmem + C::s_col(t), adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
                 }
-                ptx::mma_commit(bar(C::bSFull + t));
+                commit(C::bSFull + t);
             };
             // BF16, both tiles covering every block: the schedule without
             // range tests (each branch in this loop costs the tensor pipe:
@@ -419,7 +518,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // diagonal block of its own rows): the same loop up to tile 0's
             // last step, then one step of tile 1's.
             const int h0 = R[0].hi, h1 = R[1].hi;
-            const bool uniform = !F8 && R[0].lo == lo && R[1].lo == lo && h1 == hi &&
+            const bool uniform = !F8 && !PAIR && R[0].lo == lo && R[1].lo == lo && h1 == hi &&
                                  (h0 == hi || h0 == hi - 1);
             if (ok && uniform) {
                 for (int s = lo; s <= h0; ++s) {
@@ -439,7 +538,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             ptx::tc_fence_after();
                             if (leader) {
                                 issue_pv(t, vst, i == 1);
-                                if (s == R[t].hi) ptx::mma_commit(bar(C::bODone + t));
+                                if (s == R[t].hi) commit(C::bODone + t);
                             }
                             __syncwarp();
                         }
@@ -462,7 +561,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         ptx::tc_fence_after();
                         if (leader) {
                             issue_pv(1, (i + NSV - 1) % NSV, i == 1);
-                            ptx::mma_commit(bar(C::bODone + 1));
+                            commit(C::bODone + 1);
                         }
                         __syncwarp();
                     }
@@ -481,89 +580,58 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (s - 1 >= R[t].lo && s - 1 < R[t].hi) {
                         // O_t (+)= P_t V_{s-1} once the softmax has stored P_t.
                         if (!kv_ready) {
-                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), kph,
-                                                                      abort_flag, err, kSiteKFull));
+                            ok = __all_sync(0xffffffffu,
+                                            wait_bounded<PAIR>(bar(C::bStep + kst), kph, abort_flag,
+                                                               err, kSiteKFull));
                             if (!ok) break;
                             kv_ready = true;
                         }
-                        const uint32_t vbase = sbase + C::kVOff + vst * C::kKVBytes;
-                        const uint64_t vdesc0 = ptx::sdesc_sw128(vbase, C::kKVChunkBytes, 1024);
-                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + t), p_seen[t] & 1,
-                                                                  abort_flag, err, kSitePFull));
+                        ok = __all_sync(0xffffffffu,
+                                        wait_bounded<PAIR>(bar(C::bPFull + t), pv_done[t] & 1,
+                                                           abort_flag, err, kSitePFull));
                         if (!ok) break;
                         ptx::tc_fence_after();
                         if (leader) {
-#pragma unroll
-                            for (int kk = 0; kk < C::kPVSteps; ++kk) {
-                                const uint64_t bdesc =
-                                    ptx::sdesc_add(vdesc0, kk * C::kPVKeys * C::kRowBytes);
-                                const uint32_t acc = (pv_done[t] > 0 || kk > 0) ? 1u : 0u;
-                                if constexpr (F8)
-                                    ptx::mma_ts_f8(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                                                   bdesc, kIdescPV, acc);
-                                else
-                                    ptx::mma_ts(tmem + C::o_col(t), tmem + C::s_col(t) + kk * 8,
-                                                bdesc, kIdescPV, acc);
-                            }
+                            issue_pv(t, vst, pv_done[t] == 0);
+                            if (s - 1 == R[t].hi - 1) commit(C::bODone + t);
                         }
                         __syncwarp();
-                        ++p_seen[t];
                         ++pv_done[t];
-                        if (s - 1 == R[t].hi - 1 && leader) ptx::mma_commit(bar(C::bODone + t));
-                        __syncwarp();
                     }
                     if (s < hi && s >= R[t].lo && s < R[t].hi) {
                         // S_t = Q_t K_s^T
                         if (!kv_ready) {
-                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), kph,
-                                                                      abort_flag, err, kSiteKFull));
+                            ok = __all_sync(0xffffffffu,
+                                            wait_bounded<PAIR>(bar(C::bStep + kst), kph, abort_flag,
+                                                               err, kSiteKFull));
                             if (!ok) break;
                             ptx::tc_fence_after();
                             kv_ready = true;
                         }
-                        const uint32_t qbase = sbase + C::kQOff + t * C::kQTileBytes;
-                        const uint32_t kbase = sbase + C::kKOff + kst * C::kKVBytes;
-                        if (leader) {
-                            const uint64_t adesc0 = ptx::sdesc_sw128(qbase, 16, 1024);
-                            const uint64_t bdesc0 = ptx::sdesc_sw128(kbase, 16, 1024);
-#pragma unroll
-                            for (int kk = 0; kk < C::kQKSteps; ++kk) {
-                                const uint32_t koff = (kk / 4) * C::kQChunkBytes + (kk % 4) * 32;
-                                const uint32_t boff = (kk / 4) * C::kKVChunkBytes + (kk % 4) * 32;
-                                const uint64_t adesc = ptx::sdesc_add(adesc0, koff);
-                                const uint64_t bdesc = ptx::sdesc_add(bdesc0, boff);
-                                if constexpr (F8)
-                                    ptx::mma_ss_f8(tmem + C::s_col(t), adesc, bdesc, kIdescS,
-                                                   kk > 0 ? 1u : 0u);
-                                else
-                                    ptx::mma_ss(tmem + C::s_col(t), adesc, bdesc, kIdescS,
-                                                kk > 0 ? 1u : 0u);
-                            }
-                            ptx::mma_commit(bar(C::bSFull + t));
-                        }
+                        if (leader) issue_s(t, kst);
                         __syncwarp();
                     }
                 }
                 if (!ok) break;
                 if (!kv_ready)
-                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), kph, abort_flag,
-                                                              err, kSiteKFull));
+                    ok = __all_sync(0xffffffffu, wait_bounded<PAIR>(bar(C::bStep + kst), kph,
+                                                                    abort_flag, err, kSiteKFull));
                 if (!ok) break;
                 // K_s and V_{s-1} are released by the softmax (no commit here:
                 // each commit costs the issue stream a few hundred cycles).
             }
             // Every MMA issued above completes before tensor memory is freed.
-            if (leader) ptx::mma_commit(bar(C::bDrain));
+            if (leader) commit(C::bDrain);
             __syncwarp();
-            wait_bounded(bar(C::bDrain), 0, nullptr, err, kSiteDrain);
         }
+        if (lo < hi) wait_bounded<PAIR>(bar(C::bDrain), 0, nullptr, err, kSiteDrain);
     } else {
         // ------------------------------------------------ softmax, epilogue
         const int t = warp / 4, wq = warp % 4;
         const Range Rt = (t == 0) ? R[0] : R[1];
         const int r = wq * 32 + lane;
-        const int row = q0 + t * BM + r;
-        const int row_first = q0 + t * BM;
+        const int row_first = own_row(t);
+        const int row = row_first + r;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + C::s_col(t);
         const uint32_t o_addr = tmem + lane_base + C::o_col(t);
@@ -576,7 +644,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bool ok = true;
         const float2 c2 = make_float2(scale_log2, scale_log2);
         for (int j = Rt.lo; j < Rt.hi; ++j, ++c) {
-            const bool got = wait_bounded(bar(C::bSFull + t), c & 1, abort_flag, err, kSiteSFull);
+            const bool got = wait_bounded<PAIR>(bar(C::bSFull + t), c & 1, abort_flag, err,
+                                                kSiteSFull);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             // Release K_j and V_{j-1}. In issue order PV_0(j-1), S_0(j),
             // PV_1(j-1), S_1(j), the last MMA of step j that reads either is
@@ -684,14 +753,17 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(C::bPFull + t));
+            if (lane == 0) {
+                if (PAIR && !issuer_cta) ptx::mbar_arrive_cluster(lead_bar(C::bPFull + t));
+                else ptx::mbar_arrive(bar(C::bPFull + t));
+            }
             const float2 a01 = __fadd2_rn(acc0, acc1), a23 = __fadd2_rn(acc2, acc3);
             const float2 asum = __fadd2_rn(a01, a23);
             l = fmaf(l, alpha, asum.x + asum.y);
             m_use = m_next;
         }
         if (ok && c > 0) {
-            const bool got = wait_bounded(bar(C::bODone + t), 0, abort_flag, err, kSiteODone);
+            const bool got = wait_bounded<PAIR>(bar(C::bODone + t), 0, abort_flag, err, kSiteODone);
             ok = __all_sync(0xffffffffu, got);
             ptx::tc_fence_after();
         }
@@ -754,31 +826,39 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) {
+        // Neither CTA leaves while the other may still signal its barriers
+        // or the pair's MMAs read its shared and tensor memory.
+        ptx::cluster_arrive_release();
+        ptx::cluster_wait_acquire();
+    } else {
+        __syncthreads();
+    }
     if (warp == kMmaWarp) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        if constexpr (PAIR) ptx::tmem_dealloc_pair(tmem, kTmemCols);
+        else ptx::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool PAIR>
 cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, const CUtensorMap& to, float scale_log2, float o_mul,
                      cudaStream_t stream) {
-    using C = Cfg<D, F8>;
+    using C = Cfg<D, F8, PAIR>;
     static int configured_device = -1;   // attribute is per device; set once per device seen
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(fwd_sm103_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes);
+        e = cudaFuncSetAttribute(fwd_sm103_kernel<D, F8, PAIR>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    const int pairs = (a.Nq + BM * NT - 1) / (BM * NT);
-    dim3 grid(pairs, a.H, a.B);
-    // Causal or windowed: longest pairs first within groups of heads whose
+    const int units = (a.Nq + C::kMmaM * NT - 1) / (C::kMmaM * NT);
+    dim3 grid(units * C::kCtas, a.H, a.B);
+    // Causal or windowed: longest units first within groups of heads whose
     // K and V together take about 32 MiB (a quarter of L2).
     int group_heads = 0;
     if (a.mask_kind & (kMaskCausal | kMaskWindow)) {
@@ -787,20 +867,35 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
         const long long g = std::max(1LL, (32LL << 20) / std::max(kv_head, 1LL));
         group_heads = static_cast<int>(std::min(g, nbh));
     }
-    fwd_sm103_kernel<D, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(
-        tq, tk, tv, to, a.lse, a.H, a.Nq, a.Nk, scale_log2, o_mul,
-        a.mask_kind, a.window, a.seqlens_k, a.err, group_heads);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if constexpr (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fwd_sm103_kernel<D, F8, PAIR>, tq, tk, tv, to, a.lse, a.H,
+                              a.Nq, a.Nk, scale_log2, o_mul, a.mask_kind, a.window, a.seqlens_k,
+                              a.err, group_heads);
 }
 
 }  // namespace
 
+// pair: the CTA-pair kernel (d = 128; tk then has boxes of 64 keys).
 cudaError_t launch_fwd_sm103_maps(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                                  const CUtensorMap& tv, const CUtensorMap& to,
+                                  const CUtensorMap& tv, const CUtensorMap& to, bool pair,
                                   cudaStream_t stream) {
     const float sl2 = a.scale * kLog2e;
-    return a.d == 64 ? launch_d<64, false>(a, tq, tk, tv, to, sl2, 1.f, stream)
-                     : launch_d<128, false>(a, tq, tk, tv, to, sl2, 1.f, stream);
+    if (a.d == 64) return launch_d<64, false, false>(a, tq, tk, tv, to, sl2, 1.f, stream);
+    return pair ? launch_d<128, false, true>(a, tq, tk, tv, to, sl2, 1.f, stream)
+                : launch_d<128, false, false>(a, tq, tk, tv, to, sl2, 1.f, stream);
 }
 
 // E4M3 inputs, d = 128: the score scale folds the Q and K dequantisation
@@ -810,7 +905,7 @@ cudaError_t launch_fwd_fp8_maps(const FwdArgs& a, float descale_q, float descale
                                 const CUtensorMap& tv, const CUtensorMap& to,
                                 cudaStream_t stream) {
     const float sl2 = a.scale * descale_q * descale_k * kLog2e;
-    return launch_d<128, true>(a, tq, tk, tv, to, sl2, descale_v, stream);
+    return launch_d<128, true, false>(a, tq, tk, tv, to, sl2, descale_v, stream);
 }
 
 }  // namespace attn
