@@ -51,9 +51,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the source file of the kernel and its
 # SHA-256 at capture time; reported as null when the source has changed.
-FWD_SHA = "4178639fb660ab722899a927c57ff1276818cc2c50efe1db6560ca42867619f6"
+FWD_SHA = "2159ebea0c65cb7105881063f847ad559272b334db5572d99a38204219969f18"
 DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
-BWD_SHA = "dd91f3180f1e946c45efeb6fdb38f78c27338bffd1fb4cbadddc259339dc7c37"
+BWD_SHA = "f050930247eff6a5a393e1c9f10a821499e2874c85b7ff45698f9e0484b17655"
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
     # launch at the full bench workload, 1-pass ncu capture; valid while the
@@ -74,9 +74,10 @@ NCU_TRAFFIC = {
                "bytes_per_launch": 2147542528 + 3053312 + 1072640,
                "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split and combine kernels)"},
     "backward": {"file": "bwd_sm103.cu", "sha256": BWD_SHA,
-                 "bytes_per_launch": (270548992 + 5424640) + (541174528 + 237196544) +
-                                     (541544192 + 115900416),
-                 "workload": "prefill_B1_H64_N8192_d128_bf16 backward (prep, dK/dV and dQ kernels)"},
+                 "bytes_per_launch": (270567424 + 219403520) + (810055936 + 488616960) +
+                                     (268467968 + 86580480),
+                 "workload": "prefill_B1_H64_N8192_d128_bf16 backward (prep, dK/dV/dQ and "
+                             "dQ convert kernels)"},
     "softmax": {"file": "softmax.cu",
                 "sha256": "9a40d74a21d385c58919240ac5c54e555e31ccc3e2bd568868bc0f51f562068d",
                 "bytes_per_launch": 537604096 + 475967488,
@@ -474,16 +475,16 @@ def run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
     do = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
     o, lse = attn.attn_fwd(q, k, v, mask_kind=w.mask_kind)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(attn.attn_bwd_workspace_bytes(w.B, w.H, w.Nq, w.d), dtype=torch.uint8,
-                     device=dev)
+    ws = torch.empty(attn.attn_bwd_workspace_bytes(w.B, w.H, w.Nq, w.d, lib=args.fwd_lib),
+                     dtype=torch.uint8, device=dev)
 
     def step_b():
         attn.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, mask_kind=w.mask_kind,
-                      workspace=ws, stream=stream)
+                      workspace=ws, stream=stream, lib=args.fwd_lib)
 
     b_steps = max(3, args.steps // 4)
     b_total, b_per = time_loop(step_b, b_steps, args.warmup, stream, dist_on)
-    attn.attn_check_device_error(stream)
+    attn.attn_check_device_error(stream, lib=args.fwd_lib)
     b_total = max_over_ranks(b_total, dist_on)
     fl = 2.5 * flops(w)          # five products of 2 d FLOPs per visible pair
     b_ms = statistics.mean(b_per)
@@ -492,8 +493,8 @@ def run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
         "metric": "attn bwd TFLOP/s", "config": w.describe(),
         "ms_per_step": round(b_total / b_steps, 4),
         "value": round(whole_job_rate(fl, world, b_steps, b_total) / 1e12, 2), "unit": "TFLOP/s",
-        "flop_count": "2.5x forward (5 products: S, dP, dV, dK, dQ); the kernels execute 7 "
-                      "(S and dP are recomputed for dQ)",
+        "flop_count": "2.5x forward (5 products: S, dP, dV, dK, dQ); at d = 128 the kernels "
+                      "execute exactly these (dQ accumulated by the keys-outer kernel)",
         "gpu_launches_per_step": 3,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -785,8 +786,8 @@ def main():
     ap.add_argument("--softmax-rows", type=int, default=0,
                     help="override the row count of the softmax workload")
     ap.add_argument("--lib", default=None,
-                    help="another build of libattn.so for the forward sections (one made by "
-                         "python -m online_softmax_02_gb300.build -D ... --out PATH)")
+                    help="another build of libattn.so for the forward and backward sections (one "
+                         "made by python -m online_softmax_02_gb300.build -D ... --out PATH)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

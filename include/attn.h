@@ -224,7 +224,9 @@ attn_status_t attn_fwd_f32(const float* q, const float* k, const float* v,
  * attn_bwd_workspace_bytes -- bytes of scratch attn_bwd needs: two FP32
  * values (the row's log-sum-exp in log2 units and D = <dO, O>) per query
  * row, rows rounded up to a multiple of 128 per (b, h), in two 256-byte
- * aligned regions. Returns 0 for invalid arguments.
+ * aligned regions; at d = 128 also an FP32 dQ accumulator of d values per
+ * such row (for B=1, H=64, Nq=8192: 256 MiB). Returns 0 for invalid
+ * arguments.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int d);
 
@@ -236,9 +238,13 @@ size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int d);
  * "What interviewers probe next", on what the backward pass stores; P2
  * "A strong answer", closing paragraph). With D_i = <dO_i, O_i>:
  *   dV = P^T dO,  dS = P * (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q.
- * Three launches on `stream`: D and lse into the workspace; a keys-outer
- * kernel accumulating dK and dV in tensor memory; a queries-outer kernel
- * accumulating dQ in tensor memory (S and dP are recomputed there).
+ * Three launches on `stream`. d = 128: D and lse into the workspace (and
+ * the dQ accumulator zeroed); a keys-outer kernel accumulating dK and dV in
+ * tensor memory and adding each key block's dQ contribution into the FP32
+ * accumulator in the workspace; dQ = scale * accumulator to BF16. The order
+ * of those additions is not fixed, so dQ may differ in its last bit between
+ * runs (dK, dV are reproducible). d = 64: D and lse; the keys-outer kernel
+ * for dK, dV; a queries-outer kernel for dQ (S and dP recomputed there).
  *
  *   q, k, v      device BF16, as for attn_fwd.
  *   o            device BF16 [B,H,Nq,d]: the forward output.

@@ -216,17 +216,20 @@ def attn_fwd_f32(q, k, v, o=None, lse=None, scale=None, mask_kind=MASK_NONE, win
                 window, seqlens_k, stream)
 
 
-def attn_bwd_workspace_bytes(B: int, H: int, Nq: int, d: int) -> int:
-    return int(load().attn_bwd_workspace_bytes(B, H, Nq, d))
+def attn_bwd_workspace_bytes(B: int, H: int, Nq: int, d: int, lib=None) -> int:
+    return int((lib or load()).attn_bwd_workspace_bytes(B, H, Nq, d))
 
 
 def attn_bwd(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, scale=None,
-             mask_kind=MASK_NONE, window=0, seqlens_k=None, workspace=None, stream=None):
+             mask_kind=MASK_NONE, window=0, seqlens_k=None, workspace=None, stream=None,
+             lib=None):
     """Attention backward through ``attn_bwd``: BF16 q, k, v [B,H,N,d], the
     forward's BF16 output o and FP32 lse [B,H,Nq], and the BF16 gradient
-    dout of the loss with respect to o. Returns (dq, dk, dv) in BF16."""
+    dout of the loss with respect to o. Returns (dq, dk, dv) in BF16.
+    ``lib``: a handle from ``open_build`` (default: the library next to this
+    file)."""
     import torch
-    lib = load()
+    lib = lib or load()
     _require(q, "q", torch.bfloat16)
     dev = q.device
     for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
@@ -258,7 +261,7 @@ def attn_bwd(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, scale=None,
                           _ptr(dk), _ptr(dv), B, H, Nq, Nk, d, float(scale), int(mask_kind),
                           int(window), _ptr(seqlens_k), _ptr(workspace), workspace.numel(),
                           _stream_handle(stream, dev))
-    _check(st)
+    _check(st, lib)
     return dq, dk, dv
 
 

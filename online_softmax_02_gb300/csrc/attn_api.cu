@@ -573,7 +573,9 @@ size_t bwd_region(int B, int H, int Nq) {
 
 ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int Nq, int d) {
     if (B < 0 || H < 0 || Nq < 0 || (d != 64 && d != 128)) return 0;
-    return 2 * bwd_region(B, H, Nq);
+    // lse and D rows; with dQ accumulated in the keys-outer kernel, an FP32
+    // dQ accumulator of d values per (padded) query row after them
+    return 2 * bwd_region(B, H, Nq) + (bwd_fused_dq(d) ? bwd_region(B, H, Nq) * d : 0);
 }
 
 ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -625,8 +627,11 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
     if ((st = encode_3d(&tv64, v, d, Nk, bh, false, 64)) != ATTN_OK) return st;
     float* ws_lse2 = static_cast<float*>(workspace);
     float* ws_dd = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_region(B, H, Nq));
+    float* ws_dq = bwd_fused_dq(d) ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                              2 * bwd_region(B, H, Nq))
+                                   : nullptr;
     BwdArgs a{q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, mask_kind, window,
-              seqlens_k, ws_lse2, ws_dd, err};
+              seqlens_k, ws_lse2, ws_dd, ws_dq, err};
     e = launch_bwd(a, tq, tk, tv, tdo, tk64, tv64, s);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_bwd kernel launch");
 }

@@ -10,24 +10,37 @@
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
 //   dK = scale dS^T Q,  dQ = scale dS K.
 //
-// Three launches:
+// Three launches (d = 128):
 //   bwd_prep_kernel   D_i and LSE_i * log2(e) per query row into the
 //                     workspace, rows padded to a multiple of 128 (padding
-//                     rows get LSE = +inf, D = 0, so they contribute P = 0).
+//                     rows get LSE = +inf, D = 0, so they contribute P = 0);
+//                     zeroes the FP32 dQ accumulator.
 //   bwd_dkdv_kernel   keys outer: a CTA owns 128 keys of one (b, h) and walks
 //                     the query blocks in units of 64 queries. Per unit:
 //                     S^T = K Q_u^T and dP^T = V dO_u^T (M = 128 keys, N = 64)
 //                     into one of two tensor-memory buffers; one thread per
 //                     key row turns them into P^T and dS^T (BF16, written back
-//                     into the buffer); dV += P^T dO_u and dK += dS^T Q_u
-//                     accumulate in tensor memory (A operand from TMEM).
+//                     into the buffer, dS^T also into shared memory); then
+//                     dQ_u^T = K^T dS_u^T (M = d, N = 64: the unit's dQ,
+//                     transposed, into the buffer's dP^T columns, which are
+//                     read by then), dV += P^T dO_u and dK += dS^T Q_u
+//                     (A operand from TMEM) accumulate in tensor memory. Four
+//                     dQ warps read dQ_u^T out and add it into the FP32
+//                     accumulator with red.global.add (one 128-byte line per
+//                     warp instruction). Five products per unit, none
+//                     recomputed.
+//   bwd_dq_convert_kernel  dQ = scale * accumulator, rounded to BF16.
+// d = 64 (and builds with ATTN_BWD_FUSED_DQ=0) keep dQ in its own pass:
 //   bwd_dq_kernel     queries outer: a CTA owns 128 queries; per unit of 64
 //                     keys S = Q K_u^T, dP = dO V_u^T, dS (BF16, TMEM), and
-//                     dQ += dS K_u in tensor memory.
-// dQ is recomputed in its own pass (S and dP twice) rather than accumulated
-// with atomics: tensor memory holds the dK/dV kernel's two unit buffers
-// (4 x 64 columns) and its dK and dV accumulators (2 x 128 at d = 128), and
-// no dQ tile beside them.
+//                     dQ += dS K_u in tensor memory (S and dP computed twice:
+//                     seven products per unit pair instead of five).
+// On the prefill shape (B1 H64 8192^2 d128) the fused form measures 4.92 ms
+// per step against 5.53 ms: the dQ reductions (17 GB of FP32 partial sums
+// per step, into an accumulator that stays in L2 while a head's CTAs run)
+// cost about 0.9 ms of the 1.9 ms that dropping the two recomputed products
+// saves. The reduction order of dQ across key blocks is not fixed, so dQ may
+// differ in its last bit from run to run; dK and dV are reproducible.
 //
 // Pipelining. Two unit buffers in tensor memory per kernel (in the dQ
 // kernel K and V arrive as 64-key units in a ring of six slots, which the
@@ -49,6 +62,7 @@
 // per row (TMEM lanes 0-127), then the TMA producer warp and the MMA issuer /
 // TMEM owner warp; those two run their loops on the whole warp and issue
 // from one elected lane. Every wait is bounded.
+#include <algorithm>
 #include <climits>
 #include "common.cuh"
 
@@ -72,6 +86,12 @@ constexpr int NSB = 2;                    // ring stages
 constexpr uint32_t kTmemColsB = 512;
 constexpr float kLog2eB = 1.4426950408889634f;
 
+// Column (within a unit buffer) of the BF16 operand for K-step kk (16 rows
+// of the unit's inner dimension): each row warp writes its 32 rows' packed
+// values (16 columns) at the start of its own 32 score columns, so the two
+// warps that share a lane quarter never write columns the other still reads.
+__host__ __device__ constexpr uint32_t a_col(int kk) { return (kk / 2) * 32 + (kk % 2) * 8; }
+
 template <int D>
 struct BCfg {
     static constexpr uint32_t kRowBytes = 128;
@@ -80,33 +100,46 @@ struct BCfg {
     static constexpr uint32_t kUnitBytes = BU * kRowBytes;      // offset of the second half
 };
 
-// --- dK/dV kernel shared memory: K, V once; ring of {Q, dO, LSE2, D} ---
-template <int D>
+// --- dK/dV kernel shared memory: K, V once; ring of {Q, dO, LSE2, D};
+// with FQ (dQ accumulated here) also the unit's dS^T as the B operand of
+// dQ^T = K^T dS^T ---
+template <int D, bool FQ = false>
 struct KVCfg : BCfg<D> {
     using B = BCfg<D>;
     static constexpr uint32_t kKOff = 0;
     static constexpr uint32_t kVOff = B::kTileBytes;
-    static constexpr uint32_t kStageBytes = 2 * B::kTileBytes + 2 * BT * 4;
+    static constexpr uint32_t kRowVals = 2 * BT * 4;           // the rows' LSE and D
+    static constexpr uint32_t kStageBytes = 2 * B::kTileBytes + kRowVals;
     static constexpr uint32_t kRingOff = 2 * B::kTileBytes;
     static constexpr uint32_t q_off(int s) { return kRingOff + s * kStageBytes; }
     static constexpr uint32_t do_off(int s) { return q_off(s) + B::kTileBytes; }
     static constexpr uint32_t lse_off(int s) { return q_off(s) + 2 * B::kTileBytes; }
     static constexpr uint32_t dd_off(int s) { return lse_off(s) + BT * 4; }
-    static constexpr uint32_t kBarOff = kRingOff + NSB * kStageBytes;
+    // dS^T of one unit: 128 key rows of 64 queries (BF16), 128-byte swizzle
+    static constexpr uint32_t kDSOff = kRingOff + NSB * kStageBytes;
+    static constexpr uint32_t kDSBytes = FQ ? BT * BU * 2 : 0;
+    static constexpr uint32_t kBarOff = kDSOff + kDSBytes;
     static constexpr int kBufs = 2;       // unit buffers in tensor memory
     // per buffer: S^T done, dP^T done (MMA commits); P^T and dS^T stored
-    // (one arrival per row warp)
+    // (one arrival per row warp); FQ: dQ^T done (MMA commit; also frees the
+    // dS^T shared-memory buffer) and dQ^T read out (one arrival per dQ warp)
     static constexpr int bKV = 0, bInFull = 1, bInEmpty = 1 + NSB, bS = 1 + 2 * NSB,
-                         bDP = bS + kBufs, bDS = bDP + kBufs,
-                         bDone = bDS + kBufs, kNumBars = bDone + 1;
+                         bDP = bS + kBufs, bDS = bDP + kBufs, bDQ = bDS + kBufs,
+                         bDQFree = bDQ + kBufs, bDone = bDQFree + kBufs, kNumBars = bDone + 1;
     static constexpr uint32_t kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     // tensor memory columns: two unit buffers {S^T, dP^T} of 64 columns each,
-    // then the dV and dK accumulators
+    // then the dV and dK accumulators. FQ packs P^T into the buffer's
+    // columns 0-31 and dS^T into 32-63 (over S^T, which the row warps have
+    // read), and dQ^T (M = d rows, 64 query columns) goes into 64-127 once
+    // the row warps have read dP^T.
     static constexpr uint32_t cS(int b) { return 128u * b; }
     static constexpr uint32_t cDP(int b) { return 128u * b + BU; }
     static constexpr uint32_t cDV = 256, cDK = 256 + D;
+    // column of K-step kk of the P^T / dS^T operand within a unit buffer
+    static constexpr uint32_t p_col(int kk) { return FQ ? kk * 8 : a_col(kk); }
+    static constexpr uint32_t ds_col(int kk) { return FQ ? 32 + kk * 8 : BU + a_col(kk); }
 };
 
 // --- dQ kernel: Q and dO live in tensor memory; shared memory holds a ring
@@ -139,12 +172,6 @@ struct QCfg : BCfg<D> {
     static_assert(cDO + D / 2 <= kTmemColsB, "tensor memory budget");
 };
 
-// Column (within a unit buffer) of the BF16 operand for K-step kk (16 rows
-// of the unit's inner dimension): each row warp writes its 32 rows' packed
-// values (16 columns) at the start of its own 32 score columns, so the two
-// warps that share a lane quarter never write columns the other still reads.
-__host__ __device__ constexpr uint32_t a_col(int kk) { return (kk / 2) * 32 + (kk % 2) * 8; }
-
 __device__ __forceinline__ bool visible(int q, int key, int Lk, bool causal, bool windowed,
                                         int window) {
     bool vis = key < Lk;
@@ -162,7 +189,8 @@ template <int D>
 __global__ void __launch_bounds__(256)
 bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                 const float* __restrict__ lse, float* __restrict__ ws_lse2,
-                float* __restrict__ ws_dd, int Nq, int Nq_pad, long long rows_pad) {
+                float* __restrict__ ws_dd, float* __restrict__ ws_dq, int Nq, int Nq_pad,
+                long long rows_pad) {
     constexpr int kLanesPerRow = D / 8;
     static_assert(32 % kLanesPerRow == 0, "rows must not straddle warps");
     const long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -187,6 +215,12 @@ bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __rest
 #pragma unroll
     for (int off = kLanesPerRow / 2; off >= 1; off >>= 1)
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (in && ws_dq != nullptr) {
+        // the dQ accumulator row starts at zero (8 values per lane)
+        float4* z = reinterpret_cast<float4*>(ws_dq + wrow * D + sub * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (in && sub == 0) {
         if (real) {
             const float l = lse[bh * Nq + i];
@@ -201,15 +235,30 @@ bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __rest
 }
 
 // ---------------------------------------------------------------- dK, dV
-template <int D>
-__global__ void __launch_bounds__(kThreadsB, 1)
+// FQ: dQ is accumulated here too. After dV and dK, each unit also issues
+// dQ_u^T = K^T dS_u^T (M = d, N = 64 queries, A = K read MN-major from its
+// tile, B = dS_u^T from shared memory, which the row warps write beside the
+// tensor-memory copy), and four dQ warps read the result out of tensor
+// memory and add it into the FP32 dQ workspace with red.global.add (one
+// warp instruction covers 32 consecutive head dims of one query row: 128
+// contiguous bytes). The dQ accumulation order across key blocks is not
+// fixed, so dQ may differ in its last bits from run to run.
+template <bool FQ>
+constexpr int dkdv_threads() { return (kRowWarpsB + 2 + (FQ ? 4 : 0)) * 32; }
+constexpr int kDQWarp0 = kRowWarpsB + 2;
+
+template <int D, bool FQ>
+__global__ void __launch_bounds__(dkdv_threads<FQ>(), 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const float* __restrict__ ws_lse2, const float* __restrict__ ws_dd,
-                __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int H, int Nq,
+                float* __restrict__ ws_dq, __nv_bfloat16* __restrict__ dk,
+                __nv_bfloat16* __restrict__ dv, int H, int Nq,
                 int Nk, int Nq_pad, float scale_log2, float scale, int mask_kind, int window,
                 const int* __restrict__ seqlens_k, unsigned int* __restrict__ err) {
-    using C = KVCfg<D>;
+    static_assert(!FQ || (D == 128 && kRowWarpsB == 4),
+                  "dQ in the keys-outer kernel: d = 128, four row warps (each owns a lane quarter)");
+    using C = KVCfg<D, FQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -249,6 +298,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ptx::mbar_init(bar(C::bS + u), 1);
             ptx::mbar_init(bar(C::bDP + u), 1);
             ptx::mbar_init(bar(C::bDS + u), kRowWarpsB);   // one arrival per row warp
+            ptx::mbar_init(bar(C::bDQ + u), 1);
+            ptx::mbar_init(bar(C::bDQFree + u), 4);          // one arrival per dQ warp
         }
         ptx::mbar_init(bar(C::bDone), 1);
         *abort_flag = 0;
@@ -286,7 +337,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!__all_sync(0xffffffffu, got)) break;
                 if (leader) {
                     const int q0 = (ilo + i) * BT;
-                    ptx::mbar_arrive_expect_tx(bar(C::bInFull + st), 2 * C::kTileBytes + 2 * BT * 4);
+                    ptx::mbar_arrive_expect_tx(bar(C::bInFull + st), 2 * C::kTileBytes + C::kRowVals);
                     for (int c = 0; c < D / 64; ++c) {
                         ptx::tma_load_3d(sbase + C::q_off(st) + c * C::kChunkBytes, &tm_q,
                                          bar(C::bInFull + st), c * 64, q0, bh);
@@ -319,15 +370,13 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // u - 1, and G(u - 1) (dV, dK) follows as soon as they are done.
             static_assert(C::kBufs == 2, "G(u - 1) follows S(u); buffer = query half");
             auto do_s = [&](int i, int hh) {         // S^T, dP^T of unit 2 i + hh
-                const int st = i % NSB, bf = hh;
+                const int st = i % NSB, bf = hh, u = 2 * i + hh;
+                // S^T = K Q_hh^T and dP^T = V dO_hh^T (M = 128 keys, N = 64 queries)
+                const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
+                const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
                 if (leader) {
-                    // S^T = K Q_hh^T and dP^T = V dO_hh^T (M = 128 keys, N = 64 queries)
-                    const uint32_t qh = sbase + C::q_off(st) + hh * C::kUnitBytes;
-                    const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
                     const uint64_t kd0 = ptx::sdesc_sw128(sbase + C::kKOff, 16, 1024);
-                    const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::kVOff, 16, 1024);
                     const uint64_t qd0 = ptx::sdesc_sw128(qh, 16, 1024);
-                    const uint64_t dd0 = ptx::sdesc_sw128(dh, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
@@ -335,6 +384,22 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                     ptx::sdesc_add(qd0, off), kIdS, kk > 0 ? 1u : 0u);
                     }
                     ptx::mma_commit(bar(C::bS + bf));
+                }
+                __syncwarp();
+                if constexpr (FQ) {
+                    // dP^T goes where dQ^T of unit u - 2 was: wait until the
+                    // dQ warps have read it out
+                    if (u >= 2) {
+                        const bool got = __all_sync(
+                            0xffffffffu, wait_bounded(bar(C::bDQFree + bf), ((u - 2) / 2) & 1,
+                                                      abort_flag, err, kSiteODone));
+                        if (!got) return false;
+                        ptx::tc_fence_after();
+                    }
+                }
+                if (leader) {
+                    const uint64_t vd0 = ptx::sdesc_sw128(sbase + C::kVOff, 16, 1024);
+                    const uint64_t dd0 = ptx::sdesc_sw128(dh, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
@@ -344,8 +409,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ptx::mma_commit(bar(C::bDP + bf));
                 }
                 __syncwarp();
+                return true;
             };
-            auto do_g = [&](int i, int hh) {         // dV, dK of unit v = 2 i + hh
+            auto do_g = [&](int i, int hh) {         // dV, dK (and dQ^T) of unit v = 2 i + hh
                 const int v = 2 * i + hh, st = i % NSB, bf = hh;
                 // one wait for both products: dS^T stored implies P^T stored
                 const bool got = __all_sync(0xffffffffu,
@@ -358,16 +424,33 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t dh = sbase + C::do_off(st) + hh * C::kUnitBytes;
                     const uint64_t qg0 = ptx::sdesc_sw128(qh, C::kChunkBytes, 1024);
                     const uint64_t dg0 = ptx::sdesc_sw128(dh, C::kChunkBytes, 1024);
+                    if constexpr (FQ) {
+                        // dQ_v^T = K^T dS_v^T (M = d, N = 64 queries, K = 128 keys):
+                        // A = K MN-major (head-dim atoms 16 KiB apart), B = dS^T
+                        // from shared memory; 16 keys (2 KiB of rows) per step.
+                        // Issued first: its completion frees the shared dS^T
+                        // buffer for the next unit's row warps and starts the
+                        // dQ warps' read-out.
+                        constexpr uint32_t kIdQ = ptx::idesc_bf16_f32_amn(D, BU, true);
+                        const uint64_t ka0 = ptx::sdesc_sw128(sbase + C::kKOff, C::kChunkBytes, 1024);
+                        const uint64_t sa0 = ptx::sdesc_sw128(sbase + C::kDSOff, C::kDSBytes, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < BT / 16; ++kk)
+                            ptx::mma_ss(tmem + C::cDP(bf), ptx::sdesc_add(ka0, kk * 16 * C::kRowBytes),
+                                        ptx::sdesc_add(sa0, kk * 16 * C::kRowBytes), kIdQ,
+                                        kk > 0 ? 1u : 0u);
+                        ptx::mma_commit(bar(C::bDQ + bf));
+                    }
                     // dV += P^T dO_hh (A from TMEM, B MN-major, K = 64 queries)
 #pragma unroll
                     for (int kk = 0; kk < BU / 16; ++kk)
-                        ptx::mma_ts(tmem + C::cDV, tmem + C::cS(bf) + a_col(kk),
+                        ptx::mma_ts(tmem + C::cDV, tmem + C::cS(bf) + C::p_col(kk),
                                     ptx::sdesc_add(dg0, kk * 16 * C::kRowBytes), kIdG,
                                     (v > 0 || kk > 0) ? 1u : 0u);
                     // dK += dS^T Q_hh
 #pragma unroll
                     for (int kk = 0; kk < BU / 16; ++kk)
-                        ptx::mma_ts(tmem + C::cDK, tmem + C::cDP(bf) + a_col(kk),
+                        ptx::mma_ts(tmem + C::cDK, tmem + C::cS(bf) + C::ds_col(kk),
                                     ptx::sdesc_add(qg0, kk * 16 * C::kRowBytes), kIdG,
                                     (v > 0 || kk > 0) ? 1u : 0u);
                     // after the block's second unit, its Q/dO stage is free
@@ -385,18 +468,50 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             };
             // Block by block: S(2i), G(2i - 1), S(2i + 1), G(2i); the loop
             // body has no tests beyond the waits' own.
-            if (ok && (ok = wait_in(0))) { do_s(0, 0); do_s(0, 1); ok = do_g(0, 0); }
+            if (ok && (ok = wait_in(0)) && (ok = do_s(0, 0)) && (ok = do_s(0, 1))) ok = do_g(0, 0);
             for (int i = 1; ok && i < nblk; ++i) {
                 if (!(ok = wait_in(i))) break;
-                do_s(i, 0);
+                if (!(ok = do_s(i, 0))) break;
                 if (!(ok = do_g(i - 1, 1))) break;
-                do_s(i, 1);
+                if (!(ok = do_s(i, 1))) break;
                 ok = do_g(i, 0);
             }
             if (ok) ok = do_g(nblk - 1, 1);
             if (leader) ptx::mma_commit(bar(C::bDone));
             __syncwarp();
             wait_bounded(bar(C::bDone), 0, nullptr, err, kSiteDrain);
+        }
+    } else if (FQ && warp >= kDQWarp0) {
+        // dQ warps: a warp may read only tensor-memory lane quarter warp % 4,
+        // here head dims [32 qd, 32 qd + 32) of each unit's dQ^T. After the
+        // read the columns are freed, and the unit's 64 query rows are added
+        // into the FP32 accumulator [B*H][Nq_pad][d] with red.global.add: one
+        // warp instruction covers 32 consecutive head dims of one query row,
+        // a single 128-byte line. (Measured alternatives on the prefill
+        // backward: 16-byte vector reductions into a head-dim-major
+        // accumulator, 32 lines per instruction, 7.69 ms per step; bulk
+        // tensor reductions from a shared-memory staging buffer, 7.34 ms;
+        // this form 5.13 ms, against 5.52 ms for recomputing S and dP in a
+        // separate dQ kernel.)
+        const int qd = warp % 4;
+        const int dcol = qd * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+        for (int u = 0; u < 2 * nblk; ++u) {
+            const int bf = u % C::kBufs;
+            const bool got = wait_bounded(bar(C::bDQ + bf), (u / C::kBufs) & 1, abort_flag, err,
+                                          kSiteODone);
+            if (!__all_sync(0xffffffffu, got)) break;
+            ptx::tc_fence_after();
+            uint32_t v64[64];
+            ptx::tmem_ld32x32b_x64(tmem + lane_base + C::cDP(bf), v64);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(C::bDQFree + bf));
+            const int qb = (ilo + u / 2) * BT + (u % 2) * BU;        // first query of the unit
+            float* dst = ws_dq + (static_cast<long long>(bh) * Nq_pad + qb) * D + dcol;
+#pragma unroll
+            for (int j = 0; j < BU; ++j) ptx::red_add_f32(dst + static_cast<long long>(j) * D,
+                                                          __uint_as_float(v64[j]));
         }
     } else {
         // one thread per key row
@@ -416,9 +531,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             ptx::tc_fence_after();
             const int st = i % NSB;
+            const int qb = (ilo + i) * BT + hh * BU;               // first query of the unit
             const float* lse2 = reinterpret_cast<const float*>(smem + C::lse_off(st)) + hh * BU;
             const float* dd = reinterpret_cast<const float*>(smem + C::dd_off(st)) + hh * BU;
-            const int qb = (ilo + i) * BT + hh * BU;               // first query of the unit
             const bool full_vis = (kb + BT <= Lk) && (!causal || kb + BT - 1 <= qb) &&
                                   (!windowed || kb > qb + BU - 1 - window);
             const uint32_t a_st = tmem + lane_base + C::cS(bf);
@@ -453,7 +568,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     pf[k][qi / 2] = make_float2(p0, p1);
                     pkp[qi / 2] = pack_bf16x2(p0, p1);
                 }
-                ptx::tmem_st32x32b_x16(a_st + qt * 32, pkp);
+                ptx::tmem_st32x32b_x16(a_st + C::p_col(2 * qt), pkp);
             }
             // Phase 2 (needs dP^T): dS^T = P^T (dP^T - D), BF16 into the
             // quarter's own dP^T columns; one hand-off for both P^T and dS^T
@@ -481,8 +596,29 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                    nd));
                     pks[qi / 2] = pack_bf16x2(ds.x, ds.y);
                 }
-                ptx::tmem_st32x32b_x16(a_dpt + qt * 32, pks);
+                ptx::tmem_st32x32b_x16(a_st + C::ds_col(2 * qt), pks);
+                if constexpr (FQ) {
+                    // dS^T row r also into shared memory (B operand of dQ^T):
+                    // 16-byte chunk j of the 128-byte row at j ^ (r % 8); the
+                    // buffer is free once dQ^T of the previous unit is done
+                    if (k == 0 && u > 0) {
+                        const int pu = u - 1;
+                        const bool gq = wait_bounded(bar(C::bDQ + pu % C::kBufs),
+                                                     (pu / C::kBufs) & 1, abort_flag, err,
+                                                     kSiteODone);
+                        if (!__all_sync(0xffffffffu, gq)) { ok = false; break; }
+                    }
+                    const uint32_t row_addr = sbase + C::kDSOff + r * 128;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = qt * 4 + e;
+                        ptx::st_shared_v4(row_addr + ((j ^ (r & 7)) << 4), pks[4 * e],
+                                          pks[4 * e + 1], pks[4 * e + 2], pks[4 * e + 3]);
+                    }
+                }
             }
+            if (!ok) break;
+            if constexpr (FQ) ptx::fence_proxy_async_smem();   // dS^T stores -> tensor core
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
@@ -856,29 +992,72 @@ cudaError_t set_smem(K kernel, uint32_t bytes, int* configured) {
     return e;
 }
 
+// dQ = scale * (FP32 accumulator [B*H][Nq_pad][d]) rounded to BF16 for the
+// real query rows; eight head dims per thread (two 16-byte loads, one
+// 16-byte store).
+template <int D>
+__global__ void __launch_bounds__(256)
+bwd_dq_convert_kernel(const float* __restrict__ ws_dq, __nv_bfloat16* __restrict__ dq,
+                      long long rows, int Nq, int Nq_pad, float scale) {
+    constexpr int kPer = D / 8;
+    const long long n = rows * kPer;
+    for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
+         t += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = t / kPer;            // (bh, q) over the real rows
+        const int part = static_cast<int>(t % kPer);
+        const long long bh = row / Nq;
+        const long long q = row - bh * Nq;
+        const float4* src = reinterpret_cast<const float4*>(ws_dq + (bh * Nq_pad + q) * D + part * 8);
+        const float4 a = src[0], b = src[1];
+        uint4 w;
+        w.x = pack_bf16x2(a.x * scale, a.y * scale);
+        w.y = pack_bf16x2(a.z * scale, a.w * scale);
+        w.z = pack_bf16x2(b.x * scale, b.y * scale);
+        w.w = pack_bf16x2(b.z * scale, b.w * scale);
+        *reinterpret_cast<uint4*>(dq + row * D + part * 8) = w;
+    }
+}
+
+#ifndef ATTN_BWD_FUSED_DQ
+#define ATTN_BWD_FUSED_DQ 1
+#endif
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,
                          const CUtensorMap& tv64, cudaStream_t stream) {
+    constexpr bool FQ = (D == 128) && ATTN_BWD_FUSED_DQ != 0;
     static int cfg_kv = -1, cfg_q = -1;
-    cudaError_t e = set_smem(bwd_dkdv_kernel<D>, KVCfg<D>::kSmemBytes, &cfg_kv);
+    cudaError_t e = set_smem(bwd_dkdv_kernel<D, FQ>, KVCfg<D, FQ>::kSmemBytes, &cfg_kv);
     if (e != cudaSuccess) return e;
-    e = set_smem(bwd_dq_kernel<D>, QCfg<D>::kSmemBytes, &cfg_q);
-    if (e != cudaSuccess) return e;
+    if (!FQ) {
+        e = set_smem(bwd_dq_kernel<D>, QCfg<D>::kSmemBytes, &cfg_q);
+        if (e != cudaSuccess) return e;
+    }
     const int Nq_pad = (a.Nq + BT - 1) / BT * BT;
     const long long rows_pad = static_cast<long long>(a.B) * a.H * Nq_pad;
     const float scale_log2 = a.scale * kLog2eB;
     const long long prep_threads = rows_pad * (D / 8);
+    float* ws_dq = FQ ? a.ws_dq : nullptr;
     bwd_prep_kernel<D><<<static_cast<unsigned>((prep_threads + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-        a.ws_lse2, a.ws_dd, a.Nq, Nq_pad, rows_pad);
+        a.ws_lse2, a.ws_dd, ws_dq, a.Nq, Nq_pad, rows_pad);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     dim3 g1((a.Nk + BT - 1) / BT, a.H, a.B);
-    bwd_dkdv_kernel<D><<<g1, kThreadsB, KVCfg<D>::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, a.ws_lse2, a.ws_dd, static_cast<__nv_bfloat16*>(a.dk),
+    bwd_dkdv_kernel<D, FQ><<<g1, dkdv_threads<FQ>(), KVCfg<D, FQ>::kSmemBytes, stream>>>(
+        tq, tk, tv, tdo, a.ws_lse2, a.ws_dd, ws_dq, static_cast<__nv_bfloat16*>(a.dk),
         static_cast<__nv_bfloat16*>(a.dv), a.H, a.Nq, a.Nk, Nq_pad, scale_log2, a.scale,
         a.mask_kind, a.window, a.seqlens_k, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (FQ) {
+        const long long rows = static_cast<long long>(a.B) * a.H * a.Nq;
+        const long long threads = rows * (D / 8);
+        const unsigned blocks =
+            static_cast<unsigned>(std::min<long long>((threads + 255) / 256, 152LL * 16));
+        bwd_dq_convert_kernel<D><<<blocks, 256, 0, stream>>>(
+            ws_dq, static_cast<__nv_bfloat16*>(a.dq), rows, a.Nq, Nq_pad, a.scale);
+        return cudaGetLastError();
+    }
     dim3 g2((a.Nq + BT - 1) / BT, a.H, a.B);
     bwd_dq_kernel<D><<<g2, kThreadsB, QCfg<D>::kSmemBytes, stream>>>(
         static_cast<const __nv_bfloat16*>(a.q), tk64, tv64,
@@ -888,6 +1067,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 }
 
 }  // namespace
+
+bool bwd_fused_dq(int d) { return d == 128 && ATTN_BWD_FUSED_DQ != 0; }
 
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,

@@ -136,8 +136,13 @@ struct BwdArgs {
     const int* seqlens_k;
     float* ws_lse2;    // [B*H][Nq rounded up to 128]
     float* ws_dd;      // same shape
+    float* ws_dq;      // [B*H][Nq rounded up to 128][d] FP32 dQ accumulator, or NULL when
+                       // dQ has its own kernel (see bwd_fused_dq)
     unsigned int* err;
 };
+// True when attn_bwd accumulates dQ inside the keys-outer kernel for head
+// dimension d (and so needs the FP32 dQ workspace).
+bool bwd_fused_dq(int d);
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,
                        const CUtensorMap& tv64, cudaStream_t stream);

@@ -754,7 +754,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if (PAIR && !issuer_cta) ptx::mbar_arrive_cluster(lead_bar(C::bPFull + t));
+                if constexpr (PAIR) ptx::mbar_arrive_cluster(lead_bar(C::bPFull + t));
                 else ptx::mbar_arrive(bar(C::bPFull + t));
             }
             const float2 a01 = __fadd2_rn(acc0, acc1), a23 = __fadd2_rn(acc2, acc3);

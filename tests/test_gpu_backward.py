@@ -100,3 +100,35 @@ def test_bwd_full_size_sampled_heads(cuda_lib):
             x["v"][:, sl].float().numpy(), do[:, sl].float().numpy(), w.scale)
         for n, g, r in (("dq", dq[:, sl], rq), ("dk", dk[:, sl], rk), ("dv", dv[:, sl], rv)):
             _check(n, g, r)
+
+
+def test_bwd_three_kernel_build_d128(cuda_lib):
+    """The backward built with dQ in its own queries-outer kernel (S and dP
+    recomputed there, ATTN_BWD_FUSED_DQ=0; the form d = 64 always uses)
+    against the oracle at d = 128."""
+    import os
+    from online_softmax_02_gb300 import build as B
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    bdir = os.path.join(root, "_build", "attn_bwd3")
+    lib = cuda_lib.open_build(B.build(extra_flags=("-DATTN_BWD_FUSED_DQ=0",),
+                                      out=os.path.join(bdir, "libattn_bwd3.so"),
+                                      build_dir=os.path.join(bdir, "_objs")))
+    for (Bn, H, Nq, Nk, d, mk, win, sr) in [(2, 2, 300, 300, 128, W.MASK_CAUSAL, 0, None),
+                                            (2, 3, 400, 400, 128, W.MASK_WINDOW | W.MASK_PADDING,
+                                             100, (0, 400))]:
+        x = W.random_inputs(Bn, H, Nq, Nk, d, seed=Nq + Nk, seqlen_range=sr)
+        dev = torch.device("cuda:0")
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        sl = x["seqlens_k"].to(dev) if x.get("seqlens_k") is not None else None
+        g = torch.Generator("cpu").manual_seed(7)
+        do = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+        o, lse = cuda_lib.attn_fwd(q, k, v, mask_kind=mk, window=win, seqlens_k=sl)
+        dq, dk, dv = cuda_lib.attn_bwd(q, k, v, o, do.to(dev), lse, mask_kind=mk, window=win,
+                                       seqlens_k=sl, lib=lib)
+        cuda_lib.attn_check_device_error(lib=lib)
+        refs = OB.attention_backward(x["q"].float().numpy(), x["k"].float().numpy(),
+                                     x["v"].float().numpy(), do.float().numpy(),
+                                     1.0 / math.sqrt(d), mk, win,
+                                     None if sl is None else x["seqlens_k"].numpy())
+        for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+            _check(name, got.float().cpu().numpy(), ref)

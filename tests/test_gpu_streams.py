@@ -74,6 +74,15 @@ def test_cuda_graph_replay_matches_eager(cuda_lib):
         graph.replay()
     torch.cuda.synchronize()
     cuda_lib.attn_check_device_error()
-    for got, ref in zip((o, lse, dq, dk, dv, od, ld), eager):
-        assert torch.equal(got, ref)
+    for name, got, ref in zip(("o", "lse", "dq", "dk", "dv", "od", "ld"),
+                              (o, lse, dq, dk, dv, od, ld), eager):
+        if name == "dq":
+            # dQ sums one FP32 contribution per key block in whatever order
+            # the blocks' reductions reach memory: equal up to that order,
+            # i.e. within one BF16 rounding step of the result
+            diff = (got.float() - ref.float()).abs()
+            assert torch.all(diff <= 2.0 ** -7 * ref.float().abs() +
+                             1e-3 * ref.float().abs().max()), name
+        else:
+            assert torch.equal(got, ref), name
     assert not np.isnan(o.float().cpu().numpy()).any()
