@@ -440,10 +440,10 @@ def run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result):
 
     def step_f():
         attn.attn_fwd_fp8(q, k, v, x["descale_q"], x["descale_k"], x["descale_v"], o=o, lse=lse,
-                          stream=stream)
+                          stream=stream, lib=args.fwd_lib)
 
     f_total, f_per = time_loop(step_f, args.steps, args.warmup, stream, dist_on)
-    attn.attn_check_device_error(stream)
+    attn.attn_check_device_error(stream, lib=args.fwd_lib)
     f_total = max_over_ranks(f_total, dist_on)
     fl = flops(w)
     achieved = fl / (statistics.mean(f_per) * 1e-3) / 1e12
@@ -786,7 +786,7 @@ def main():
     ap.add_argument("--softmax-rows", type=int, default=0,
                     help="override the row count of the softmax workload")
     ap.add_argument("--lib", default=None,
-                    help="another build of libattn.so for the forward and backward sections (one "
+                    help="another build of libattn.so for the forward, E4M3 and backward sections (one "
                          "made by python -m online_softmax_02_gb300.build -D ... --out PATH)")
     args = ap.parse_args()
     if args.warmup < 3:
