@@ -224,9 +224,10 @@ template <int D, bool F8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                 float* __restrict__ lse, int H, int Nq, int Nk, float scale_log2, float o_mul,
-                 int mask_kind, int window, const int* __restrict__ seqlens_k,
-                 unsigned int* __restrict__ err, int group_heads) {
+                 __nv_bfloat16* __restrict__ o_ptr, float* __restrict__ lse, int H, int Nq, int Nk,
+                 float scale_log2, float o_mul, int mask_kind, int window,
+                 const int* __restrict__ seqlens_k, unsigned int* __restrict__ err,
+                 int group_heads) {
     using C = Cfg<D, F8, PAIR>;
     constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
     extern __shared__ uint8_t smem_raw[];
@@ -290,7 +291,23 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         R[t] = tile_range(q0 + t * C::kMmaM, C::kMmaM, Nq, Lk, causal, windowed, window);
         if (R[t].lo < R[t].hi) { lo = min(lo, R[t].lo); hi = max(hi, R[t].hi); }
     }
-    if (hi == 0) lo = 0;
+    if (hi == 0) {
+        // No row of this CTA (or pair) sees a key: O = 0 and lse = -inf for
+        // its rows, written directly -- no barriers, tensor memory or loads.
+        // (Under padding and sliding windows a large share of CTAs are empty.)
+        __nv_bfloat16* ob = o_ptr + static_cast<long long>(bh) * Nq * D;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int r0 = own_row(t);
+            const int rows = max(0, min(BM, Nq - r0));
+            uint4* dst = reinterpret_cast<uint4*>(ob + static_cast<long long>(r0) * D);
+            for (int e = threadIdx.x; e < rows * D / 8; e += kThreads) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+            if (lse != nullptr)
+                for (int e = threadIdx.x; e < rows; e += kThreads)
+                    lse[static_cast<long long>(bh) * Nq + r0 + e] = -INFINITY;
+        }
+        return;
+    }
     int nq = 0;           // tiles that see some key (their Q is loaded)
 #pragma unroll
     for (int t = 0; t < NT; ++t) nq += (R[t].lo < R[t].hi) ? 1 : 0;
@@ -881,9 +898,10 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, fwd_sm103_kernel<D, F8, PAIR>, tq, tk, tv, to, a.lse, a.H,
-                              a.Nq, a.Nk, scale_log2, o_mul, a.mask_kind, a.window, a.seqlens_k,
-                              a.err, group_heads);
+    return cudaLaunchKernelEx(&cfg, fwd_sm103_kernel<D, F8, PAIR>, tq, tk, tv, to,
+                              static_cast<__nv_bfloat16*>(a.o), a.lse, a.H, a.Nq, a.Nk,
+                              scale_log2, o_mul, a.mask_kind, a.window, a.seqlens_k, a.err,
+                              group_heads);
 }
 
 }  // namespace
