@@ -491,8 +491,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // backward: 16-byte vector reductions into a head-dim-major
         // accumulator, 32 lines per instruction, 7.69 ms per step; bulk
         // tensor reductions from a shared-memory staging buffer, 7.34 ms;
-        // this form 5.13 ms, against 5.52 ms for recomputing S and dP in a
-        // separate dQ kernel.)
+        // lane pairs swapping values to issue 8-byte reductions, two lines
+        // per instruction, 5.16 ms; this form 4.92-5.13 ms, against 5.52 ms
+        // for recomputing S and dP in a separate dQ kernel.)
         const int qd = warp % 4;
         const int dcol = qd * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
