@@ -51,24 +51,24 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the source file of the kernel and its
 # SHA-256 at capture time; reported as null when the source has changed.
-FWD_SHA = "2159ebea0c65cb7105881063f847ad559272b334db5572d99a38204219969f18"
+FWD_SHA = "fc5aee8faaef4ea53e3943fe010db9c46daf714cd21f22406a5823820904863e"
 DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
-BWD_SHA = "f050930247eff6a5a393e1c9f10a821499e2874c85b7ff45698f9e0484b17655"
+BWD_SHA = "2fe8dae0db309cbe9ce496463fe2583c8f287d59f286961a1a963e5bf4875034"
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
     # launch at the full bench workload, 1-pass ncu capture; valid while the
     # kernel source is unchanged.
     "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                 "bytes_per_launch": 403099136 + 116022272,
+                 "bytes_per_launch": 403243520 + 116358656,
                  "workload": "prefill_B1_H64_N8192_d128_bf16"},
     "fwd_bf16_causal": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                        "bytes_per_launch": 403559424 + 115297792,
+                        "bytes_per_launch": 403867392 + 115645952,
                         "workload": "causal_B2_H32_N8192_d128_bf16"},
     "fwd_bf16_masked": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                        "bytes_per_launch": 243448832 + 109369088,
+                        "bytes_per_launch": 244009728 + 109795584,
                         "workload": "masked_B8_H16_N4096_d128_bf16_window1024_padded"},
     "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                 "bytes_per_launch": 201975808 + 104190976,
+                 "bytes_per_launch": 201452544 + 104424704,
                  "workload": "prefill_B1_H64_N8192_d128_e4m3"},
     "decode": {"file": "decode.cu", "sha256": DECODE_SHA,
                "bytes_per_launch": 2147542528 + 3053312 + 1072640,
