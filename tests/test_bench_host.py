@@ -101,3 +101,14 @@ def test_traffic_records_follow_their_source_hash(monkeypatch):
                         dict(bench.NCU_TRAFFIC["fwd_bf16"], sha256="0" * 64))
     assert bench.traffic_for("fwd_bf16") is None
     assert bench.traffic_for("no such kernel") is None
+
+
+def test_build_cli_needs_out_with_options():
+    """A build with compile-time options must name its own library (the
+    default libattn.so is never overwritten by an option build)."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-m", "online_softmax_02_gb300.build", "-D",
+                        "ATTN_FWD_PAIR=1"], capture_output=True, text=True,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode != 0 and "--out" in r.stderr
