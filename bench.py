@@ -457,6 +457,10 @@ def run_fp8_section(args, rank, world, dist_on, dev, stream, peaks, result):
                      "unit": "TFLOP/s", "frac": round(achieved / peak8, 4),
                      "traffic": traffic_for("fwd_e4m3", w.H / W.PREFILL.H),
                      "peak_note": "measured bf16 burst x 2 (nominal e4m3 / bf16 dense ratio)"}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xr = {n: (x[n].float() * x["descale_" + n]) for n in ("q", "k", "v")}
+        result["fp8"]["cpu_baseline"] = cpu_baseline(w, xr, o, lse, args, args.cpu_seconds / 4)
+        result["fp8"]["cpu_baseline"]["sample"] += " (E4M3 inputs dequantised exactly to FP32)"
     del q, k, v, o, lse, x
     return run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
 
@@ -501,6 +505,8 @@ def run_backward_section(args, rank, world, dist_on, dev, stream, peaks, result)
                      "frac": round(achieved / peaks["bf16_tflops"], 4),
                      "traffic": traffic_for("backward", w.H / W.PREFILL.H),
                      "note": "time and DRAM traffic of the three launches per step"}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["backward"]["cpu_baseline"] = cpu_baseline_backward(w, x, do, dq, dk, dv)
     del q, k, v, do, o, lse, dq, dk, dv, ws, x
     return run_decode_section(args, rank, world, dist_on, dev, stream, peaks, result)
 
@@ -578,6 +584,8 @@ def run_softmax_section(args, rank, world, dist_on, dev, stream, peaks, result):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                      "traffic": traffic_for("softmax", x.shape[0] / W.SOFTMAX_ROWS)}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["softmax"]["cpu_baseline"] = cpu_baseline_softmax(x, y, lse, args.cpu_seconds / 4)
     del x, y, lse
     if not args.no_naive:
         result["softmax"]["naive_attention_context"] = naive_attention_context(args, dev, stream,
@@ -729,6 +737,58 @@ def cpu_baseline_decode(w, x, o_gpu, lse_gpu, seconds):
                       % (nh - 1, w.H, w.Nk),
             "max_abs_err_gpu_vs_oracle": float(np.abs(got - ro).max()),
             "max_abs_lse_err_gpu_vs_oracle": float(np.abs(got_l - rl).max())}
+
+
+def cpu_baseline_backward(w, x, do, dq, dk, dv):
+    """The FP64 backward oracle (numpy) on the first head of the workload
+    (every query and key of it), in the backward metric's unit, with its
+    normwise agreement with the GPU gradients of that head."""
+    from oracle import backward as OB
+    one = [x[n][:1, :1].float().numpy() for n in ("q", "k", "v")]
+    t0 = time.perf_counter()
+    rq, rk, rv = OB.attention_backward(*one, do[:1, :1].float().cpu().numpy(), w.scale,
+                                       w.mask_kind, w.window)
+    dt = time.perf_counter() - t0
+    fl = 2.5 * 4.0 * w.d * w.Nq * w.Nk        # one head, no mask
+    errs = {}
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        g = got[:1, :1].float().cpu().numpy()
+        errs["normwise_err_" + name] = float(np.abs(g - ref).max() / np.abs(ref).max())
+    try:
+        import threadpoolctl
+        cores = max(p.get("num_threads", 1) for p in threadpoolctl.threadpool_info())
+    except Exception:   # noqa: BLE001
+        cores = len(os.sched_getaffinity(0))
+    return dict({"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                 "kind": "oracle", "seconds": round(dt, 2),
+                 "sample": "head 0 of %d (all %d queries and keys) of the %s backward"
+                           % (w.H, w.Nq, w.name)}, **errs)
+
+
+def cpu_baseline_softmax(x, y, lse, seconds):
+    """The FP64 row-softmax oracle on the first rows of the workload (as many
+    as fit in about `seconds`), in GB/s of the rows' algorithmic bytes, with
+    its agreement with the GPU rows."""
+    import oracle
+    orc = oracle.Oracle()
+    threads = oracle.default_threads()
+    n = x.shape[1]
+
+    def run(r):
+        xs = x[:r].float().cpu().numpy()
+        t0 = time.perf_counter()
+        ry, rl = orc.softmax_rows(xs, threads=threads)
+        return ry, rl, time.perf_counter() - t0
+
+    _, _, dt1 = run(16)
+    r = int(min(x.shape[0], max(16, 16 * seconds / max(dt1, 1e-3))))
+    ry, rl, dt = run(r)
+    alg = r * (2 * n * x.element_size() + 4)
+    return {"value": round(alg / dt / 1e9, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": "rows 0..%d of %d (all %d values each)" % (r - 1, x.shape[0], n),
+            "max_abs_err_gpu_vs_oracle": float(np.abs(y[:r].cpu().numpy() - ry).max()),
+            "max_abs_lse_err_gpu_vs_oracle": float(np.abs(lse[:r].cpu().numpy() - rl).max())}
 
 
 def run_reference(args, rank, world):
