@@ -172,14 +172,6 @@ struct QCfg : BCfg<D> {
     static_assert(cDO + D / 2 <= kTmemColsB, "tensor memory budget");
 };
 
-__device__ __forceinline__ bool visible(int q, int key, int Lk, bool causal, bool windowed,
-                                        int window) {
-    bool vis = key < Lk;
-    if (causal) vis = vis && key <= q;
-    if (windowed) vis = vis && key > q - window;
-    return vis;
-}
-
 // ---------------------------------------------------------------- prep
 // D = <dO_i, O_i> and LSE * log2(e) per query row. D / 8 lanes share a row,
 // each reading 16 bytes of O and of dO (a warp covers 32 * 16 B of each per
@@ -537,6 +529,18 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const float* dd = reinterpret_cast<const float*>(smem + C::dd_off(st)) + hh * BU;
             const bool full_vis = (kb + BT <= Lk) && (!causal || kb + BT - 1 <= qb) &&
                                   (!windowed || kb > qb + BU - 1 - window);
+            // this key's visible queries in the unit: one interval [qb + ja, qb + je)
+            int ja = 0;
+            unsigned vspan = BU;
+            if (!full_vis) {
+                int je = BU;
+                if (causal) ja = max(ja, key - qb);
+                if (windowed)
+                    je = static_cast<int>(min(static_cast<long long>(je),
+                                              static_cast<long long>(key) + window - qb));
+                if (key >= Lk) je = ja;
+                vspan = static_cast<unsigned>(max(je - ja, 0));
+            }
             const uint32_t a_st = tmem + lane_base + C::cS(bf);
             const uint32_t a_dpt = tmem + lane_base + C::cDP(bf);
             // Phase 1 (needs S^T): P^T = exp2(S^T c - lse2) for this warp's
@@ -562,9 +566,9 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         make_float2(__uint_as_float(sv[qi]), __uint_as_float(sv[qi + 1])), c2, nl);
                     float p0 = ptx::ex2(x.x), p1 = ptx::ex2(x.y);
                     if (!full_vis) {
-                        const int qg = qb + qt * 32 + qi;
-                        if (!visible(qg, key, Lk, causal, windowed, window)) p0 = 0.f;
-                        if (!visible(qg + 1, key, Lk, causal, windowed, window)) p1 = 0.f;
+                        const int jq = qt * 32 + qi;
+                        if (static_cast<unsigned>(jq - ja) >= vspan) p0 = 0.f;
+                        if (static_cast<unsigned>(jq + 1 - ja) >= vspan) p1 = 0.f;
                     }
                     pf[k][qi / 2] = make_float2(p0, p1);
                     pkp[qi / 2] = pack_bf16x2(p0, p1);
@@ -895,6 +899,15 @@ bwd_dq_kernel(const __nv_bfloat16* __restrict__ qg, const __grid_constant__ CUte
             const int kb0 = (jlo + j) * BT + hh * BU;               // first key of the unit
             const bool full_vis = (kb0 + BU <= Lk) && (!causal || kb0 + BU - 1 <= q0) &&
                                   (!windowed || kb0 > q0 + BT - 1 - window);
+            // this query's visible keys in the unit: one interval [kb0 + ka, kb0 + ke)
+            int ka = 0;
+            unsigned vspan = BU;
+            if (!full_vis) {
+                int ke = min(BU, Lk - kb0);
+                if (causal) ke = min(ke, row + 1 - kb0);
+                if (windowed) ka = max(ka, row - window + 1 - kb0);
+                vspan = static_cast<unsigned>(max(ke - ka, 0));
+            }
             const uint32_t a_s = tmem + lane_base + C::cS(bf);
             const uint32_t a_dp = tmem + lane_base + C::cDP(bf);
             // P for this warp's keys (quarters of 32) as soon as S is done,
@@ -912,9 +925,9 @@ bwd_dq_kernel(const __nv_bfloat16* __restrict__ qg, const __grid_constant__ CUte
                         make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), c2, nl2);
                     float p0 = ptx::ex2(x.x), p1 = ptx::ex2(x.y);
                     if (!full_vis) {
-                        const int key = kb0 + kt * 32 + kk;
-                        if (!visible(row, key, Lk, causal, windowed, window)) p0 = 0.f;
-                        if (!visible(row, key + 1, Lk, causal, windowed, window)) p1 = 0.f;
+                        const int jk = kt * 32 + kk;
+                        if (static_cast<unsigned>(jk - ka) >= vspan) p0 = 0.f;
+                        if (static_cast<unsigned>(jk + 1 - ka) >= vspan) p1 = 0.f;
                     }
                     pf[k][kk / 2] = make_float2(p0, p1);
                 }

@@ -681,14 +681,15 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ptx::tmem_ld32x32b_x128(s_addr, sr);
             const int kb = j * BN;
             if (block_needs_mask(kb, row_first, Lk, causal, windowed, window)) {
+                // the row's visible keys in this block are one interval
+                // [kb + a, kb + e): one unsigned comparison per key
+                int a = 0, e = min(BN, Lk - kb);
+                if (causal) e = min(e, row + 1 - kb);
+                if (windowed) a = max(0, row - window + 1 - kb);
+                const unsigned span = static_cast<unsigned>(max(e - a, 0));
 #pragma unroll
-                for (int kk = 0; kk < BN; ++kk) {
-                    const int key = kb + kk;
-                    bool vis = key < Lk;
-                    if (causal) vis = vis && key <= row;
-                    if (windowed) vis = vis && key > row - window;
-                    if (!vis) sr[kk] = __float_as_uint(-INFINITY);
-                }
+                for (int kk = 0; kk < BN; ++kk)
+                    if (static_cast<unsigned>(kk - a) >= span) sr[kk] = __float_as_uint(-INFINITY);
             }
             // row max: four independent chains of three-input max
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
