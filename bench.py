@@ -51,31 +51,31 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the source file of the kernel and its
 # SHA-256 at capture time; reported as null when the source has changed.
-FWD_SHA = "fc5aee8faaef4ea53e3943fe010db9c46daf714cd21f22406a5823820904863e"
+FWD_SHA = "1a0d76317be57fe60270611de6eb514a1b688533a8ffb1f93b924e280dcdd90c"
 DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
-BWD_SHA = "2fe8dae0db309cbe9ce496463fe2583c8f287d59f286961a1a963e5bf4875034"
+BWD_SHA = "c47d5c0b04f877d8cb5b8dcbc7b72c99c5d4157365c91755eb893bdd8f751e83"
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
     # launch at the full bench workload, 1-pass ncu capture; valid while the
     # kernel source is unchanged.
     "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                 "bytes_per_launch": 403243520 + 116358656,
+                 "bytes_per_launch": 402899456 + 114624000,
                  "workload": "prefill_B1_H64_N8192_d128_bf16"},
     "fwd_bf16_causal": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                        "bytes_per_launch": 403867392 + 115645952,
+                        "bytes_per_launch": 403515136 + 115045888,
                         "workload": "causal_B2_H32_N8192_d128_bf16"},
     "fwd_bf16_masked": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                        "bytes_per_launch": 244009728 + 109795584,
+                        "bytes_per_launch": 243665408 + 109755648,
                         "workload": "masked_B8_H16_N4096_d128_bf16_window1024_padded"},
     "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                 "bytes_per_launch": 201452544 + 104424704,
+                 "bytes_per_launch": 201450240 + 104258048,
                  "workload": "prefill_B1_H64_N8192_d128_e4m3"},
     "decode": {"file": "decode.cu", "sha256": DECODE_SHA,
                "bytes_per_launch": 2147542528 + 3053312 + 1072640,
                "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split and combine kernels)"},
     "backward": {"file": "bwd_sm103.cu", "sha256": BWD_SHA,
-                 "bytes_per_launch": (270567424 + 219403520) + (810055936 + 488616960) +
-                                     (268467968 + 86580480),
+                 "bytes_per_launch": (270547456 + 219994880) + (809643008 + 488216064) +
+                                     (268460544 + 86488064),
                  "workload": "prefill_B1_H64_N8192_d128_bf16 backward (prep, dK/dV/dQ and "
                              "dQ convert kernels)"},
     "softmax": {"file": "softmax.cu",
