@@ -174,8 +174,8 @@ struct Cfg {
     static constexpr uint32_t kBarOff = kVOff + kStagesV * kSlotBytes;
     // barrier indices (pair: QFull, Step and PFull are used in the first
     // CTA only, where the MMAs are issued; the others in both)
-    static constexpr int bQFull = 0;
-    static constexpr int bStep = 1;                    // [NSK]: step s has K_s and V_{s-1}
+    static constexpr int bQFull = 0;                   // [NT]: tile t's Q landed
+    static constexpr int bStep = bQFull + NT;          // [NSK]: step s has K_s and V_{s-1}
     static constexpr int bKEmpty = bStep + kStagesK;
     static constexpr int bVEmpty = bKEmpty + kStagesK;
     static constexpr int bSFull = bVEmpty + kStagesV;
@@ -259,12 +259,14 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int units = gridDim.x / C::kCtas;
     int unit = blockIdx.x / C::kCtas, h = blockIdx.y, b = blockIdx.z;
     if (group_heads > 0) {
+        // 32-bit arithmetic (the launcher keeps the grid below 2^31 CTAs; a
+        // 64-bit division is a long software sequence on the CTA's start-up
+        // path)
         const int nbh = gridDim.y * gridDim.z;
-        const long long lin = unit + static_cast<long long>(units) *
-                                         (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
-        const long long per_group = static_cast<long long>(group_heads) * units;
-        const int g = static_cast<int>(lin / per_group);
-        const int idx = static_cast<int>(lin - g * per_group);
+        const int lin = unit + units * (blockIdx.y + gridDim.y * blockIdx.z);
+        const int per_group = group_heads * units;
+        const int g = lin / per_group;
+        const int idx = lin - g * per_group;
         const int gh = min(group_heads, nbh - g * group_heads);   // heads in this group
         unit = units - 1 - idx / gh;
         const int bhl = g * group_heads + idx % gh;
@@ -308,35 +310,42 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         return;
     }
-    int nq = 0;           // tiles that see some key (their Q is loaded)
-#pragma unroll
-    for (int t = 0; t < NT; ++t) nq += (R[t].lo < R[t].hi) ? 1 : 0;
+    // Tile 1 starting inside tile 0's range, one or more blocks later (a
+    // sliding window): its first S product is issued at the start of that
+    // step, ahead of tile 0's P V product of the previous block, so that its
+    // softmax does not wait for tile 0's first one. That step's K and V
+    // blocks are then last read by tile 0's S product, and tile 0's softmax
+    // releases them (see the release rule below).
+    const int early_s = (!PAIR && R[1].lo > R[0].lo && R[1].lo < R[0].hi && R[1].lo < R[1].hi)
+                            ? R[1].lo : -1;
     // This CTA's Q tiles, loaded into its own shared memory; completion is
     // counted on the issuing CTA's barrier. Only tiles that see some key: an
     // empty tile's buffer is written by its epilogue straight away and must
     // not receive a late Q.
-    auto load_q = [&]() {
-        ptx::prefetch_tmap(&tm_q);
-        for (int t = 0; t < NT; ++t) {
-            if (R[t].lo >= R[t].hi) continue;
-            for (int c = 0; c < C::kChunks; ++c) {
-                const uint32_t dst = sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes;
-                if constexpr (PAIR)
-                    ptx::tma_load_3d_pair(dst, &tm_q, lead_bar(C::bQFull), c * C::kChunkElems,
-                                          own_row(t), bh);
-                else
-                    ptx::tma_load_3d(dst, &tm_q, bar(C::bQFull), c * C::kChunkElems, own_row(t), bh);
-            }
+    auto load_q = [&](int t) {
+        if (R[t].lo >= R[t].hi) return;
+        for (int c = 0; c < C::kChunks; ++c) {
+            const uint32_t dst = sbase + C::kQOff + t * C::kQTileBytes + c * C::kQChunkBytes;
+            if constexpr (PAIR)
+                ptx::tma_load_3d_pair(dst, &tm_q, lead_bar(C::bQFull + t), c * C::kChunkElems,
+                                      own_row(t), bh);
+            else
+                ptx::tma_load_3d(dst, &tm_q, bar(C::bQFull + t), c * C::kChunkElems, own_row(t), bh);
         }
     };
 
-    // The Q tiles are the first thing the CTA needs and the longest load it
-    // waits for: the thread that sets up the barriers starts them before the
-    // tensor-memory allocation and the block-wide barrier (pair: the second
-    // CTA's, which count on the first CTA's barrier, after the cluster
-    // barrier that publishes its initialisation).
+    // The Q tiles and the first K block are the first things the CTA needs
+    // and the longest loads it waits for: the thread that sets up the
+    // barriers starts them before the tensor-memory allocation and the
+    // block-wide barrier (pair: the second CTA's Q, which counts on the
+    // first CTA's barrier, after the cluster barrier that publishes its
+    // initialisation; the pair's K blocks all come from the producer loop).
+    // One CTA: K_lo goes into slot 0 of the K ring on step barrier 0, as the
+    // producer loop would load it (a fresh ring has every slot free), right
+    // after tile 0's Q: with one Q barrier per tile, tile 0's first S product
+    // waits for 64 KiB (BF16) instead of both Q tiles and K_lo.
     if (warp == kProducerWarp && lane == 0) {
-        ptx::mbar_init(bar(C::bQFull), 1);
+        for (int t = 0; t < NT; ++t) ptx::mbar_init(bar(C::bQFull + t), 1);
         for (int s = 0; s < NSK; ++s) {
             ptx::mbar_init(bar(C::bStep + s), 2);            // the K and the V producer
             ptx::mbar_init(bar(C::bKEmpty + s), 1);
@@ -351,8 +360,20 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         *abort_flag = 0;
         ptx::fence_mbar_init();
         if (lo < hi && issuer_cta) {
-            ptx::mbar_arrive_expect_tx(bar(C::bQFull), nq * C::kCtas * C::kQTileBytes);
-            load_q();
+            ptx::prefetch_tmap(&tm_q);
+            for (int t = 0; t < NT; ++t) {
+                if (R[t].lo < R[t].hi) {
+                    ptx::mbar_arrive_expect_tx(bar(C::bQFull + t), C::kCtas * C::kQTileBytes);
+                    load_q(t);
+                }
+                if (!PAIR && t == 0) {
+                    ptx::prefetch_tmap(&tm_k);
+                    ptx::mbar_arrive_expect_tx(bar(C::bStep), C::kKVBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        ptx::tma_load_3d(sbase + C::kKOff + c * C::kKChunkBytes, &tm_k, bar(C::bStep),
+                                         c * C::kChunkElems, lo * BN, bh);
+                }
+            }
         }
     }
     if (warp == kMmaWarp) {
@@ -368,7 +389,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if constexpr (PAIR) {
         ptx::cluster_arrive_release();
         ptx::cluster_wait_acquire();
-        if (warp == kProducerWarp && lane == 0 && lo < hi && !issuer_cta) load_q();
+        if (warp == kProducerWarp && lane == 0 && lo < hi && !issuer_cta) {
+            ptx::prefetch_tmap(&tm_q);
+            for (int t = 0; t < NT; ++t) load_q(t);
+        }
     } else {
         __syncthreads();
     }
@@ -403,7 +427,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int b = is_k ? i : i - 1;      // block this producer adds to step i
                 const bool load = b >= 0 && b < n;
                 const uint32_t sb = bar(C::bStep + i % NSK);
-                if (load) {
+                if (!PAIR && is_k && b == 0) {
+                    issued = 1;                      // started with the Q tiles
+                } else if (load) {
                     const int st = b % ns;
                     const bool got = wait_bounded(bar(empty0 + st), ((b / ns) & 1) ^ 1, abort_flag,
                                                   err, is_k ? kSiteKEmpty : kSiteVEmpty);
@@ -452,8 +478,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // (bounded: a step's phase also needs the other producer).
                 if (issuer_cta) {
                     if (is_k)
-                        wait_bounded<PAIR>(bar(C::bQFull), 0, nullptr, err, kSiteDrain,
-                                           kWaitLimitCycles / 8);
+                        for (int t = 0; t < NT; ++t)
+                            if (R[t].lo < R[t].hi)
+                                wait_bounded<PAIR>(bar(C::bQFull + t), 0, nullptr, err, kSiteDrain,
+                                                   kWaitLimitCycles / 8);
                     for (int b = max(0, issued - ns); b < issued; ++b) {
                         const int i = is_k ? b : b + 1;
                         wait_bounded<PAIR>(bar(C::bStep + i % NSK), (i / NSK) & 1, nullptr, err,
@@ -487,8 +515,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int pv_done[NT];
 #pragma unroll
             for (int t = 0; t < NT; ++t) pv_done[t] = 0;
-            bool ok = __all_sync(0xffffffffu, wait_bounded<PAIR>(bar(C::bQFull), 0, abort_flag, err,
-                                                                 kSiteQFull));
+            bool ok = true;
             // O_t (+)= P_t V_{s-1} (A = P_t from tensor memory) and S_t = Q_t K_s^T.
             auto issue_pv = [&](int t, int vst, bool first) {
                 const uint32_t vbase = sbase + C::kVOff + vst * C::kSlotBytes;
@@ -537,28 +564,40 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int h0 = R[0].hi, h1 = R[1].hi;
             const bool uniform = !F8 && !PAIR && R[0].lo == lo && R[1].lo == lo && h1 == hi &&
                                  (h0 == hi || h0 == hi - 1);
-            if (ok && uniform) {
-                for (int s = lo; s <= h0; ++s) {
+            if (uniform) {
+                // step 0, peeled: S_0 once Q_0 and K_lo have landed, S_1 once
+                // Q_1 has too (tile 1's Q arrives last)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (t == 0)
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep), 0, abort_flag, err,
+                                                                  kSiteKFull));
+                    if (ok)
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQFull + t), 0, abort_flag,
+                                                                  err, kSiteQFull));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (leader) issue_s(t, 0);
+                    __syncwarp();
+                }
+                for (int s = lo + 1; ok && s <= h0; ++s) {
                     const int i = s - lo;
                     const int kst = i % NSK;
                     const int vst = (i + NSV - 1) % NSV;
                     ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), (i / NSK) & 1,
                                                               abort_flag, err, kSiteKFull));
                     if (!ok) break;
-                    if (i == 0) ptx::tc_fence_after();   // later steps: the P wait's fence
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
-                        if (i > 0) {
-                            ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + t), (i - 1) & 1,
-                                                                      abort_flag, err, kSitePFull));
-                            if (!ok) break;
-                            ptx::tc_fence_after();
-                            if (leader) {
-                                issue_pv(t, vst, i == 1);
-                                if (s == R[t].hi) commit(C::bODone + t);
-                            }
-                            __syncwarp();
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + t), (i - 1) & 1,
+                                                                  abort_flag, err, kSitePFull));
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        if (leader) {
+                            issue_pv(t, vst, i == 1);
+                            if (s == R[t].hi) commit(C::bODone + t);
                         }
+                        __syncwarp();
                         if (s < R[t].hi) {
                             if (leader) issue_s(t, kst);
                             __syncwarp();
@@ -592,6 +631,19 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // The step barrier (K_s and V_{s-1} landed) is waited right
                 // before the step's first MMA, and once per step in any case.
                 bool kv_ready = false;
+                if (s == early_s) {
+                    // S_1 = Q_1 K_s^T first: tile 1 has no earlier block
+                    ok = __all_sync(0xffffffffu, wait_bounded<PAIR>(bar(C::bStep + kst), kph,
+                                                                    abort_flag, err, kSiteKFull));
+                    if (ok)
+                        ok = __all_sync(0xffffffffu, wait_bounded<PAIR>(bar(C::bQFull + 1), 0,
+                                                                        abort_flag, err, kSiteQFull));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    kv_ready = true;
+                    if (leader) issue_s(1, kst);
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (s - 1 >= R[t].lo && s - 1 < R[t].hi) {
@@ -615,8 +667,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         __syncwarp();
                         ++pv_done[t];
                     }
-                    if (s < hi && s >= R[t].lo && s < R[t].hi) {
-                        // S_t = Q_t K_s^T
+                    if (s < hi && s >= R[t].lo && s < R[t].hi && !(t == 1 && s == early_s)) {
+                        // S_t = Q_t K_s^T (the tile's first: once its Q has landed)
                         if (!kv_ready) {
                             ok = __all_sync(0xffffffffu,
                                             wait_bounded<PAIR>(bar(C::bStep + kst), kph, abort_flag,
@@ -624,6 +676,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             if (!ok) break;
                             ptx::tc_fence_after();
                             kv_ready = true;
+                        }
+                        if (s == R[t].lo) {
+                            ok = __all_sync(0xffffffffu, wait_bounded<PAIR>(bar(C::bQFull + t), 0,
+                                                                            abort_flag, err,
+                                                                            kSiteQFull));
+                            if (!ok) break;
+                            ptx::tc_fence_after();
                         }
                         if (leader) issue_s(t, kst);
                         __syncwarp();
@@ -669,9 +728,12 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // the S product of the last tile covering block j (tile 1 on its
             // range, tile 0 on the blocks before it: the ranges are contiguous
             // and tile 1's ends last), and its completion implies every
-            // earlier one. Nobody waits for the last blocks' releases.
-            if (wq == 0 && lane == 0 &&
-                (t == NT - 1 || !(j >= R[NT - 1].lo && j < R[NT - 1].hi))) {
+            // earlier one. At tile 1's early first block the order is S_1(j),
+            // PV_0(j-1), S_0(j), so tile 0 releases it. Nobody waits for the
+            // last blocks' releases.
+            const int releaser = (j == early_s) ? 0
+                                 : (j >= R[NT - 1].lo && j < R[NT - 1].hi) ? NT - 1 : 0;
+            if (wq == 0 && lane == 0 && t == releaser) {
                 const int ii = j - lo;
                 ptx::mbar_arrive(bar(C::bKEmpty + ii % NSK));
                 if (ii > 0) ptx::mbar_arrive(bar(C::bVEmpty + (ii - 1) % NSV));
@@ -884,6 +946,8 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
         const long long kv_head = 2LL * a.Nk * a.d * C::kElem;
         const long long g = std::max(1LL, (32LL << 20) / std::max(kv_head, 1LL));
         group_heads = static_cast<int>(std::min(g, nbh));
+        // the kernel computes this order in 32-bit arithmetic
+        if (static_cast<long long>(grid.x) * grid.y * grid.z > INT_MAX) group_heads = 0;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
