@@ -375,9 +375,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
             }
         }
-        // the O map, used by the epilogue's stores (BF16; E4M3 measured 1 %
-        // slower with it)
-        if constexpr (!F8) ptx::prefetch_tmap(&tm_o);
+        // the O map, used by the epilogue's stores (one-CTA BF16 form; E4M3
+        // measured 1 % slower with it, and the pair form spills registers)
+        if constexpr (!F8 && !PAIR) ptx::prefetch_tmap(&tm_o);
     }
     if (warp == kMmaWarp) {
         if constexpr (PAIR) {
