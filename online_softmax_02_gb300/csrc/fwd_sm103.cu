@@ -310,6 +310,18 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         return;
     }
+    // Under a causal mask tile 1 sees one key block more than tile 0: the
+    // diagonal block of its own rows, the last in key order. Walked in key
+    // order it would run alone at the end (tile 1's S -> softmax -> P V chain
+    // with nothing to overlap it); so such CTAs walk their key blocks from
+    // the last down, and the extra block becomes the first step, where tile 0
+    // is still waiting for its Q anyway. The schedule below works on steps:
+    // the ranges R[t] become step ranges (offset by lo), and blk() maps a
+    // step's block back to the key block that is loaded and masked.
+    const bool rev = !PAIR && causal && R[0].lo == lo && R[1].lo == lo && R[1].hi == hi &&
+                     R[0].hi == hi - 1;
+    if (rev) R[0] = Range{lo + 1, hi};
+    auto blk = [&](int v) { return rev ? lo + hi - 1 - v : v; };
     // Tile 1 starting inside tile 0's range, one or more blocks later (a
     // sliding window): its first S product is issued at the start of that
     // step, ahead of tile 0's P V product of the previous block, so that its
@@ -361,19 +373,23 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         ptx::fence_mbar_init();
         if (lo < hi && issuer_cta) {
             ptx::prefetch_tmap(&tm_q);
-            for (int t = 0; t < NT; ++t) {
+            auto start_q = [&](int t) {
                 if (R[t].lo < R[t].hi) {
                     ptx::mbar_arrive_expect_tx(bar(C::bQFull + t), C::kCtas * C::kQTileBytes);
                     load_q(t);
                 }
-                if (!PAIR && t == 0) {
-                    ptx::prefetch_tmap(&tm_k);
-                    ptx::mbar_arrive_expect_tx(bar(C::bStep), C::kKVBytes);
-                    for (int c = 0; c < C::kChunks; ++c)
-                        ptx::tma_load_3d(sbase + C::kKOff + c * C::kKChunkBytes, &tm_k, bar(C::bStep),
-                                         c * C::kChunkElems, lo * BN, bh);
-                }
+            };
+            // the Q of the tile whose first S comes first, the first K block,
+            // then the other Q
+            if (rev) start_q(1); else start_q(0);
+            if constexpr (!PAIR) {
+                ptx::prefetch_tmap(&tm_k);
+                ptx::mbar_arrive_expect_tx(bar(C::bStep), C::kKVBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    ptx::tma_load_3d(sbase + C::kKOff + c * C::kKChunkBytes, &tm_k, bar(C::bStep),
+                                     c * C::kChunkElems, blk(lo) * BN, bh);
             }
+            if (rev) start_q(0); else start_q(1);
         }
         // the O map, used by the epilogue's stores (one-CTA BF16 form; E4M3
         // measured 1 % slower with it, and the pair form spills registers)
@@ -450,16 +466,16 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                 for (int c = 0; c < C::kChunks; ++c)
                                     ptx::tma_load_3d_pair(dst + c * C::kKChunkBytes, map, lsb,
                                                           c * C::kChunkElems,
-                                                          (lo + b) * BN + rank * C::kKRows, bh);
+                                                          blk(lo + b) * BN + rank * C::kKRows, bh);
                             } else {
                                 ptx::tma_load_3d_pair(dst, map, lsb, rank * C::kChunkElems,
-                                                      (lo + b) * BN, bh);
+                                                      blk(lo + b) * BN, bh);
                             }
                         } else {
                             const uint32_t chunk = is_k ? C::kKChunkBytes : C::kVChunkBytes;
                             for (int c = 0; c < C::kChunks; ++c)
                                 ptx::tma_load_3d(dst + c * chunk, map, sb, c * C::kChunkElems,
-                                                 (lo + b) * BN, bh);
+                                                 blk(lo + b) * BN, bh);
                         }
                     }
                     issued = b + 1;
@@ -562,28 +578,58 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // the longer chain, measured 1.063 -> 1.098 ms with it and keeps
             // the general loop.
             // A causal tile 1 covers one block more than tile 0 (the
-            // diagonal block of its own rows): the same loop up to tile 0's
-            // last step, then one step of tile 1's.
+            // diagonal block of its own rows): walked from the last block
+            // down (rev), tile 0 starts one step later; otherwise (a window
+            // that clips neither tile) the same loop runs up to tile 0's last
+            // step, then one step of tile 1's.
             const int h0 = R[0].hi, h1 = R[1].hi;
-            const bool uniform = !F8 && !PAIR && R[0].lo == lo && R[1].lo == lo && h1 == hi &&
-                                 (h0 == hi || h0 == hi - 1);
+            const int off0 = R[0].lo - lo;          // tile 0's first step (1 when rev)
+            const bool uniform = !F8 && !PAIR && (R[0].lo == lo || rev) && R[1].lo == lo &&
+                                 h1 == hi && (h0 == hi || h0 == hi - 1);
             if (uniform) {
-                // step 0, peeled: S_0 once Q_0 and K_lo have landed, S_1 once
-                // Q_1 has too (tile 1's Q arrives last)
+                // step 0, peeled: S_t once Q_t and the first K block have
+                // landed, for the tiles that start there (tile 1's Q is loaded
+                // last, or first when rev)
+                ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep), 0, abort_flag, err,
+                                                          kSiteKFull));
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
-                    if (t == 0)
-                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep), 0, abort_flag, err,
-                                                                  kSiteKFull));
-                    if (ok)
-                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQFull + t), 0, abort_flag,
-                                                                  err, kSiteQFull));
+                    if (!ok || R[t].lo != lo) continue;
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQFull + t), 0, abort_flag,
+                                                              err, kSiteQFull));
                     if (!ok) break;
                     ptx::tc_fence_after();
                     if (leader) issue_s(t, 0);
                     __syncwarp();
                 }
-                for (int s = lo + 1; ok && s <= h0; ++s) {
+                int s_first = lo + 1;
+                if (rev && ok) {
+                    // step 1, peeled: tile 0's first S, then tile 1's first
+                    // P V product and its next S
+                    constexpr int kst = 1 % NSK, vst = 0;
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), (1 / NSK) & 1,
+                                                              abort_flag, err, kSiteKFull));
+                    if (ok)
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQFull), 0, abort_flag, err,
+                                                                  kSiteQFull));
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        if (leader) issue_s(0, kst);
+                        __syncwarp();
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + 1), 0, abort_flag,
+                                                                  err, kSitePFull));
+                    }
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        if (leader) {
+                            issue_pv(1, vst, true);
+                            issue_s(1, kst);                 // hi >= lo + 2 when rev
+                        }
+                        __syncwarp();
+                    }
+                    s_first = lo + 2;
+                }
+                for (int s = s_first; ok && s <= h0; ++s) {
                     const int i = s - lo;
                     const int kst = i % NSK;
                     const int vst = (i + NSV - 1) % NSV;
@@ -592,12 +638,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (!ok) break;
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
-                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + t), (i - 1) & 1,
+                        const int pi = i - 1 - (t == 0 ? off0 : 0);   // tile t's P hand-off index
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + t), pi & 1,
                                                                   abort_flag, err, kSitePFull));
                         if (!ok) break;
                         ptx::tc_fence_after();
                         if (leader) {
-                            issue_pv(t, vst, i == 1);
+                            issue_pv(t, vst, pi == 0);
                             if (s == R[t].hi) commit(C::bODone + t);
                         }
                         __syncwarp();
@@ -744,7 +791,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ptx::tc_fence_after();
             uint32_t sr[BN];
             ptx::tmem_ld32x32b_x128(s_addr, sr);
-            const int kb = j * BN;
+            const int kb = blk(j) * BN;
             if (block_needs_mask(kb, row_first, Lk, causal, windowed, window)) {
                 // the row's visible keys in this block are one interval
                 // [kb + a, kb + e): one unsigned comparison per key

@@ -7,8 +7,10 @@ every V block (64 head dims) and the first CTA issuing every MMA. The
 arithmetic per element is the same as the one-CTA kernel's (the same
 products in the same K order, the same softmax code), so this file checks
 the pair build against the FP64 oracle at the usual tolerances and against
-the default build bit for bit. It is not the default because it measured
-slower on GB300: every P hand-off crosses to the other SM.
+the default build bit for bit -- except under causal masks, where the
+one-CTA kernel walks a CTA's key blocks from the diagonal down and the two
+agree to rounding. It is not the default because it measured slower on
+GB300: every P hand-off crosses to the other SM.
 """
 import math
 import os
@@ -67,7 +69,16 @@ def test_pair_against_oracle_and_default(cuda_lib, pair_lib, orc, shape):
     ro, rl = oracle_fwd(orc, x, mk, win)
     assert_close(o, lse, ro, rl, TOL_O_BF16, TOL_LSE, what=str(shape))
     o0, l0 = _fwd(cuda_lib, None, x, mk, win)
-    assert np.array_equal(o, o0) and np.array_equal(lse, l0), "pair build differs from default"
+    if mk & (W.MASK_CAUSAL | W.MASK_WINDOW):
+        # the one-CTA kernel walks a causal CTA's key blocks from the diagonal
+        # down (the pair form in key order): the same sums added in another
+        # order, equal up to rounding (O: one BF16 step; lse: FP32 sums)
+        fin = np.isfinite(l0)
+        assert np.array_equal(fin, np.isfinite(lse))
+        assert np.abs(lse[fin] - l0[fin]).max(initial=0.0) <= 1e-5
+        assert np.all(np.abs(o - o0) <= 2.0 ** -7 * np.maximum(np.abs(o0), 1.0))
+    else:
+        assert np.array_equal(o, o0) and np.array_equal(lse, l0), "pair build differs from default"
 
 
 def test_pair_late_max_and_large_scores(cuda_lib, pair_lib, orc):
