@@ -46,10 +46,11 @@
 //     memory (BF16, written over S_t) and V_j from shared memory. Issue order
 //     per block: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). The MMA warp commits
 //     only S and the final O; the K and V slots are released by the softmax
-//     warp that sees the block's last S product complete. BF16 CTAs whose
-//     tiles cover the same blocks (and causal ones, up to tile 0's last
-//     block) run a straight-line version of the schedule without per-tile
-//     range tests.
+//     warp that sees the block's last S product complete. CTAs whose tiles
+//     cover the same blocks (and causal ones, whose key blocks are walked
+//     from the diagonal down so that tile 0 starts one step after tile 1)
+//     run a straight-line version of the schedule without per-tile range
+//     tests.
 //   * Warps 0-3 run the softmax of tile 0 and warps 4-7 that of tile 1, one
 //     thread per query row: tcgen05.ld of the 128 scores of its row, mask,
 //     row max (four independent three-input max chains) and row sum (packed
@@ -572,11 +573,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 commit(C::bSFull + t);
             };
-            // BF16, both tiles covering every block: the schedule without
-            // range tests (each branch in this loop costs the tensor pipe:
-            // prefill 1.315 -> 1.289 ms). The E4M3 kernel, whose softmax is
-            // the longer chain, measured 1.063 -> 1.098 ms with it and keeps
-            // the general loop.
+            // Both tiles covering every block: the schedule without range
+            // tests (each branch in this loop costs the tensor pipe: BF16
+            // prefill 1.315 -> 1.289 ms; E4M3, once its first step was
+            // peeled and each tile's Q had its own barrier, 1.108 -> 1.070 ms).
             // A causal tile 1 covers one block more than tile 0 (the
             // diagonal block of its own rows): walked from the last block
             // down (rev), tile 0 starts one step later; otherwise (a window
@@ -584,7 +584,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // step, then one step of tile 1's.
             const int h0 = R[0].hi, h1 = R[1].hi;
             const int off0 = R[0].lo - lo;          // tile 0's first step (1 when rev)
-            const bool uniform = !F8 && !PAIR && (R[0].lo == lo || rev) && R[1].lo == lo &&
+            const bool uniform = !PAIR && (R[0].lo == lo || rev) && R[1].lo == lo &&
                                  h1 == hi && (h0 == hi || h0 == hi - 1);
             if (uniform) {
                 // step 0, peeled: S_t once Q_t and the first K block have
