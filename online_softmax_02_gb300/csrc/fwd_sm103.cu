@@ -120,12 +120,16 @@ constexpr float kTau = 8.0f;
 // instruction in it shows: prefill B1 H64 8192^2 d128 1.312 / 1.319 /
 // 1.378 ms with 0 / 1 / 2 pairs (BF16), causal 0.731 / 0.744 / 0.763 ms,
 // E4M3 1.064 / 1.110 ms with 0 / 1. (An earlier build, whose softmax was
-// on the critical path, measured 1 pair fastest for BF16.)
+// on the critical path, measured 1 pair fastest for BF16.) Since the E4M3
+// kernel runs the straight-line schedule, its exponential unit is the
+// tighter resource there: E4M3 prefill 1.072 / 1.067 / 1.084 ms with
+// 0 / 1 / 2 pairs, BF16 still slower with 1. The polynomial's relative error
+// (1.0e-4) is far below P's rounding to E4M3 (2^-4).
 #ifndef ATTN_SOFT_EXP2_PAIRS_BF16
 #define ATTN_SOFT_EXP2_PAIRS_BF16 0
 #endif
 #ifndef ATTN_SOFT_EXP2_PAIRS_E4M3
-#define ATTN_SOFT_EXP2_PAIRS_E4M3 0
+#define ATTN_SOFT_EXP2_PAIRS_E4M3 1
 #endif
 template <bool F8>
 __host__ __device__ constexpr bool soft_pair(int idx) {

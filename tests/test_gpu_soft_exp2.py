@@ -4,8 +4,9 @@ P1 ("What did FlashAttention-2 and -3 change?") credits FlashAttention-4 with
 computing some of the softmax exponentials in software on the FMA units
 instead of the special-function unit. The forward kernel can do this for a
 compile-time number of every 16 exponential pairs (ATTN_SOFT_EXP2_PAIRS_BF16,
-ATTN_SOFT_EXP2_PAIRS_E4M3; 0 in the default build, where the measured best
-is to keep every exponential on the special-function unit). This file builds
+ATTN_SOFT_EXP2_PAIRS_E4M3; the default build, by measurement, keeps every
+BF16 exponential on the special-function unit and computes 1 of every 16
+E4M3 pairs in software, so test_gpu_fp8.py covers that split). This file builds
 the library a second time with two of every 16 pairs in software for both
 input types, and checks that build's forward against the FP64 oracle at the
 same tolerances as the default build, through the same C interface.
