@@ -325,7 +325,7 @@ def run_ours(args, rank, world, dist_on):
            "ms_per_step": round(e_total / e_steps, 4),
            "api": "attn_fwd_host (C ABI; host buffers, device workspace, caller's stream)",
            "head_groups": pipe.chunks, "device_slots": pipe.slots,
-           "gpu_launches_per_step": -(-w.B * w.H // -(-w.B * w.H // pipe.chunks)),
+           "gpu_launches_per_step": attn.attn_fwd_host_groups(w.B, w.H, pipe.chunks),
            "h2d_d2h_GBps": round((h2d + d2h) / (e_total / e_steps * 1e-3) / 1e9, 1)}
     # the e2e result must equal the device-resident result
     e2e["matches_device_result"] = bool(torch.equal(ho.to(dev), o))
@@ -832,7 +832,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="CPU seconds the reference arm's timed steps take in all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-chunks", type=int, default=16, help="head groups of the e2e pipeline")
+    ap.add_argument("--e2e-chunks", type=int, default=4, help="head groups of the e2e pipeline")
     ap.add_argument("--e2e-slots", type=int, default=3, help="device buffer sets of the e2e pipeline")
     # profiling helpers: run one section, or a reduced size of it
     ap.add_argument("--no-naive", action="store_true",

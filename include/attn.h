@@ -133,13 +133,26 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int Nq, int Nk, int d, int gr
                                      int slots);
 
 /*
+ * attn_fwd_host_groups -- the number of head groups (one forward kernel
+ * launch each) attn_fwd_host uses for B*H heads and `groups`: the group
+ * sizes are described there. Returns -1 for negative sizes or groups < 1,
+ * 0 when B*H is 0. Host-only; never touches the device.
+ */
+int attn_fwd_host_groups(int B, int H, int groups);
+
+/*
  * attn_fwd_host -- attn_fwd for inputs and outputs in HOST memory.
  *
  * Only Q, K, V and O cross device memory in the fused method (P1 "Derive
  * online softmax, ...", "A strong answer", the cost paragraph); this call
  * moves exactly those across the host link, overlapped with the kernel. The
- * B*H heads are cut into `groups` contiguous groups of ceil(B*H / groups)
- * heads; group g is copied into buffer set g % slots of the workspace (one
+ * B*H heads are cut into contiguous groups of at most P = ceil(B*H / groups)
+ * heads: groups of P heads, except that when B*H >= 4 P (and P >= 4) the
+ * first two groups have ceil(P/4) and ceil(P/2) heads and the last two
+ * ceil(P/2) and ceil(P/4), so that the first kernel starts after a short
+ * copy and the last copy-back follows a short kernel
+ * (attn_fwd_host_groups gives the count). Group g is copied into buffer
+ * set g % slots of the workspace (one
  * cudaMemcpyAsync per tensor), computed by the attn_fwd kernel on that
  * slot's stream, and its o and lse copied back, so that the copy-in of one
  * group, the kernel of the next and the copy-out of the previous run at the

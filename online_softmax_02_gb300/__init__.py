@@ -14,6 +14,7 @@ Functions (same names as the C entry points):
                                     attn_fwd_host (copies pipelined with the
                                     kernel by head groups)
   attn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, groups, slots)
+  attn_fwd_host_groups(B, H, groups)  head groups (kernel launches) it uses
   attn_bwd(q, k, v, o, dout, lse, ...)  backward -> (dq, dk, dv)
   attn_bwd_workspace_bytes(B, H, Nq, d)
   attn_decode_workspace_bytes(B, H, d, num_splits)
@@ -81,6 +82,8 @@ def _configure(lib):
     lib.attn_fwd_f32.restype = I
     lib.attn_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     lib.attn_fwd_host_workspace_bytes.restype = S
+    lib.attn_fwd_host_groups.argtypes = [I, I, I]
+    lib.attn_fwd_host_groups.restype = I
     lib.attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, I, I, P, S, P]
     lib.attn_fwd_host.restype = I
     lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, F, F, I, I, P, P]
@@ -356,7 +359,12 @@ def attn_decode_splitkv_noalloc(q, k, v, o, lse=None, scale=None, seqlens_k=None
     return o, lse
 
 
-def attn_fwd_host_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, groups: int = 16,
+def attn_fwd_host_groups(B: int, H: int, groups: int = 4) -> int:
+    """Number of head groups (forward kernel launches) attn_fwd_host uses."""
+    return int(load().attn_fwd_host_groups(B, H, groups))
+
+
+def attn_fwd_host_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, groups: int = 4,
                                   slots: int = 3) -> int:
     return int(load().attn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, groups, slots))
 
@@ -367,7 +375,7 @@ class HostPipeline:
     of ceil(B*H / chunks) heads each. Create it once for a shape and reuse it
     across calls ordered on one stream."""
 
-    def __init__(self, B, H, Nq, Nk, d, device=None, chunks=16, slots=3):
+    def __init__(self, B, H, Nq, Nk, d, device=None, chunks=4, slots=3):
         import torch
         self.device = torch.device("cuda") if device is None else torch.device(device)
         self.B, self.H, self.Nq, self.Nk, self.d = B, H, Nq, Nk, d
@@ -389,7 +397,7 @@ def _require_host(t, name, dtype):
 
 
 def attn_fwd_from_host(q, k, v, o, lse=None, scale=None, mask_kind=MASK_NONE, window=0,
-                       seqlens_k=None, pipeline=None, chunks=16, slots=3, stream=None):
+                       seqlens_k=None, pipeline=None, chunks=4, slots=3, stream=None):
     """Fused attention forward for inputs and outputs in host memory, through
     ``attn_fwd_host``.
 

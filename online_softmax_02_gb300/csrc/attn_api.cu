@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -297,6 +298,43 @@ attn_status_t host_streams(HostStreams** out) {
     return ATTN_OK;
 }
 
+// The groups' sizes in heads, in order: full groups of `per` heads, except
+// that when there are at least four full groups' worth of heads (and a full
+// group has 4 or more) the first two groups take a quarter and a half of a
+// full group and the last two a half and a quarter. The first kernel then
+// starts after a short copy and the last copy-back follows a short kernel:
+// the pipeline's fill and drain, when the host link is not busy both ways,
+// shrink. Prefill B1 H64 8192^2 on GB300, whose host link moves the whole
+// job (403 MB in, 136 MB out) in 2.07 ms: 16 even groups 2.38 ms, 4 groups
+// 2.60 ms even and 2.275 ms with this ramp; a longer ramp (an eighth first,
+// or halving down to one head) measured 2.28-2.46 ms -- groups of one or
+// two heads launch kernels too small to fill the GPU.
+int host_group_sizes(long long bh, long long per, long long* sizes, int cap) {
+    int n = 0;
+    auto push = [&](long long v) {
+        if (n < cap && sizes != nullptr) sizes[n] = v;
+        ++n;
+    };
+    const bool ramp = per >= 4 && bh >= 4 * per;
+    const long long quarter = (per + 3) / 4, half = (per + 1) / 2;
+    long long left = bh;
+    if (ramp) {
+        push(quarter);
+        push(half);
+        left -= 2 * (quarter + half);                 // and the mirror at the end
+    }
+    while (left > 0) {
+        const long long g = std::min(per, left);
+        push(g);
+        left -= g;
+    }
+    if (ramp) {
+        push(half);
+        push(quarter);
+    }
+    return n;
+}
+
 // lens[b * H + h] = seqlens_k[b]: one key length per head, so that any group
 // of heads is a batch of one-head problems.
 __global__ void expand_seqlens_kernel(const int* __restrict__ src, int* __restrict__ dst,
@@ -314,6 +352,14 @@ ATTN_API size_t attn_fwd_host_workspace_bytes(int B, int H, int Nq, int Nk, int 
     HostLayout L;
     if (!host_layout(B, H, Nq, Nk, d, groups, slots, &L)) return 0;
     return L.total;
+}
+
+ATTN_API int attn_fwd_host_groups(int B, int H, int groups) {
+    if (B < 0 || H < 0 || groups < 1) return -1;
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh == 0) return 0;
+    const long long g = std::min<long long>(groups, bh);
+    return host_group_sizes(bh, (bh + g - 1) / g, nullptr, 0);
 }
 
 ATTN_API attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o,
@@ -381,9 +427,13 @@ ATTN_API attn_status_t attn_fwd_host(const void* q, const void* k, const void* v
         ATTN_HOST_CHECK(cudaGetLastError(), "seqlens kernel launch");
     }
     const size_t qrow = static_cast<size_t>(Nq) * d * 2, krow = static_cast<size_t>(Nk) * d * 2;
-    for (long long c = 0; c < L.groups; ++c) {
-        const long long a = c * L.per, n = std::min(L.per, L.bh - a);
-        const int si = static_cast<int>(c % L.slots);
+    const int ngroups = host_group_sizes(L.bh, L.per, nullptr, 0);
+    std::vector<long long> sizes(static_cast<size_t>(ngroups));
+    host_group_sizes(L.bh, L.per, sizes.data(), ngroups);
+    long long a = 0;                                   // first head of group c
+    for (int c = 0; c < ngroups; a += sizes[c], ++c) {
+        const long long n = sizes[c];
+        const int si = c % L.slots;
         char* sq = ws + si * L.slot;
         char* sk = sq + L.q;
         char* sv = sk + L.kv;

@@ -176,6 +176,23 @@ def test_exp2_soft_argument_errors(lib, kw, code):
     assert lib.attn_exp2_soft(a["x"], a["y"], a["n"], None) == code
 
 
+def test_host_group_count(lib):
+    # groups of at most P = ceil(B*H / groups) heads; with B*H >= 4 P and
+    # P >= 4 the first two and the last two groups take P/4 and P/2 heads
+    assert lib.attn_fwd_host_groups(1, 64, 16) == 19      # 1, 2, 14 x 4, 2, 2, 1
+    assert lib.attn_fwd_host_groups(2, 16, 4) == 7        # 2, 4, 8, 8, 4, 4, 2
+    assert lib.attn_fwd_host_groups(1, 16, 4) == 7        # 1, 2, 4, 4, 2, 2, 1
+    assert lib.attn_fwd_host_groups(1, 64, 4) == 7        # 4, 8, 16, 16, 8, 8, 4
+    assert lib.attn_fwd_host_groups(1, 24, 4) == 7        # 2, 3, 6, 6, 2, 3, 2
+    assert lib.attn_fwd_host_groups(2, 3, 3) == 3         # P = 2: no ramp
+    assert lib.attn_fwd_host_groups(1, 64, 64) == 64      # P = 1
+    assert lib.attn_fwd_host_groups(1, 12, 2) == 2        # B*H < 4 P: no ramp
+    assert lib.attn_fwd_host_groups(1, 5, 100) == 5       # more groups than heads
+    assert lib.attn_fwd_host_groups(0, 5, 4) == 0
+    assert lib.attn_fwd_host_groups(1, 5, 0) == -1
+    assert lib.attn_fwd_host_groups(-1, 5, 4) == -1
+
+
 def test_host_workspace_size(lib):
     # 2*3 heads in groups of 2 (3 groups), 2 slots: per slot q, k, v, o BF16
     # and lse FP32 for 2 heads, each region padded to 256 bytes; then the

@@ -395,6 +395,26 @@ def test_fwd_from_host_slot_counts(cuda_lib, chunks, slots):
         assert np.array_equal(hl.numpy(), l_dev)
 
 
+@pytest.mark.parametrize("mk,sr", [(0, None), (W.MASK_CAUSAL | W.MASK_PADDING, (1, 256))])
+def test_fwd_from_host_ramped_groups(cuda_lib, mk, sr):
+    """Enough heads for the ramped group sizes (2 x 16 heads in groups of at
+    most 8: 2, 4, 8, 8, 4, 4, 2 heads): bit for bit the device result,
+    including the per-head key lengths of every group."""
+    B, H, Nq, Nk, d, chunks = 2, 16, 256, 256, 64, 4
+    assert cuda_lib.attn_fwd_host_groups(B, H, chunks) == 7
+    x = W.random_inputs(B, H, Nq, Nk, d, seed=4321, seqlen_range=sr)
+    o_dev, l_dev = run_fwd(cuda_lib, x, mk)
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    ho = torch.zeros(B, H, Nq, d, dtype=torch.bfloat16).pin_memory()
+    hl = torch.zeros(B, H, Nq, dtype=torch.float32).pin_memory()
+    cuda_lib.attn_fwd_from_host(hq, hk, hv, ho, hl, mask_kind=mk, seqlens_k=x["seqlens_k"],
+                                chunks=chunks, slots=3)
+    torch.cuda.synchronize()
+    cuda_lib.attn_check_device_error()
+    assert np.array_equal(ho.float().numpy(), o_dev)
+    assert np.array_equal(hl.numpy(), l_dev)
+
+
 def test_fwd_from_host_pageable_no_lse_and_degenerate(cuda_lib):
     """attn_fwd_host with pageable (not page-locked) host buffers, without
     lse, with more groups than heads, and with no keys at all."""
