@@ -51,7 +51,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the source file of the kernel and its
 # SHA-256 at capture time; reported as null when the source has changed.
-FWD_SHA = "04b03249d7f00ebf20fc6a3f4a9776ba960cb0d17c8d66c4747a5d98d1054b4a"
+FWD_SHA = "dc3f63a62c8cfac140dcaeb3d158dbbdd03fd769809ab51675e7987628bf3cd4"
 DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
 BWD_SHA = "c47d5c0b04f877d8cb5b8dcbc7b72c99c5d4157365c91755eb893bdd8f751e83"
 NCU_TRAFFIC = {
@@ -59,16 +59,16 @@ NCU_TRAFFIC = {
     # launch at the full bench workload, 1-pass ncu capture; valid while the
     # kernel source is unchanged.
     "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                 "bytes_per_launch": 402791936 + 115932672,
+                 "bytes_per_launch": 403139840 + 116056320,
                  "workload": "prefill_B1_H64_N8192_d128_bf16"},
     "fwd_bf16_causal": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                        "bytes_per_launch": 402736128 + 112988160,
+                        "bytes_per_launch": 402731776 + 113195776,
                         "workload": "causal_B2_H32_N8192_d128_bf16"},
     "fwd_bf16_masked": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                        "bytes_per_launch": 243810560 + 109422848,
+                        "bytes_per_launch": 243614464 + 109829120,
                         "workload": "masked_B8_H16_N4096_d128_bf16_window1024_padded"},
     "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                 "bytes_per_launch": 201417216 + 104143616,
+                 "bytes_per_launch": 201400320 + 104453632,
                  "workload": "prefill_B1_H64_N8192_d128_e4m3"},
     "decode": {"file": "decode.cu", "sha256": DECODE_SHA,
                "bytes_per_launch": 2147542528 + 3053312 + 1072640,
