@@ -668,11 +668,13 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
     }
     unsigned int* err = nullptr;
     if ((st = err_word(&err)) != ATTN_OK) return st;
-    CUtensorMap tq, tk, tv, tdo, tk64, tv64;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tk64, tv64;
     if ((st = encode_bf16_3d(&tq, q, d, Nq, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tk, k, d, Nk, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tv, v, d, Nk, bh)) != ATTN_OK) return st;
     if ((st = encode_bf16_3d(&tdo, dout, d, Nq, bh)) != ATTN_OK) return st;
+    if ((st = encode_bf16_3d(&tdk, dk, d, Nk, bh)) != ATTN_OK) return st;   // the dK/dV stores
+    if ((st = encode_bf16_3d(&tdv, dv, d, Nk, bh)) != ATTN_OK) return st;
     if ((st = encode_3d(&tk64, k, d, Nk, bh, false, 64)) != ATTN_OK) return st;   // dQ kernel units
     if ((st = encode_3d(&tv64, v, d, Nk, bh, false, 64)) != ATTN_OK) return st;
     float* ws_lse2 = static_cast<float*>(workspace);
@@ -682,7 +684,7 @@ ATTN_API attn_status_t attn_bwd(const void* q, const void* k, const void* v, con
                                    : nullptr;
     BwdArgs a{q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, mask_kind, window,
               seqlens_k, ws_lse2, ws_dd, ws_dq, err};
-    e = launch_bwd(a, tq, tk, tv, tdo, tk64, tv64, s);
+    e = launch_bwd(a, tq, tk, tv, tdo, tdk, tdv, tk64, tv64, s);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_bwd kernel launch");
 }
 

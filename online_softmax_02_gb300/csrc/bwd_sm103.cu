@@ -243,9 +243,9 @@ template <int D, bool FQ>
 __global__ void __launch_bounds__(dkdv_threads<FQ>(), 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                 const float* __restrict__ ws_lse2, const float* __restrict__ ws_dd,
-                float* __restrict__ ws_dq, __nv_bfloat16* __restrict__ dk,
-                __nv_bfloat16* __restrict__ dv, int H, int Nq,
+                float* __restrict__ ws_dq, int H, int Nq,
                 int Nk, int Nq_pad, float scale_log2, float scale, int mask_kind, int window,
                 const int* __restrict__ seqlens_k, unsigned int* __restrict__ err) {
     static_assert(!FQ || (D == 128 && kRowWarpsB == 4),
@@ -634,14 +634,20 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ptx::tc_fence_after();
         }
         const bool have = ok && nblk > 0;
-        const long long orow = (static_cast<long long>(bh) * Nk + key) * D;
+        // dV and dK leave through the V and K tiles (free once every MMA is
+        // done) in the 128-byte-swizzled layout those arrived in -- 16-byte
+        // piece j of key row r at j ^ (r % 8) -- and one TMA store per 64
+        // head dims. (Each thread storing its own key row straight to global
+        // memory touched 32 lines per warp instruction: 5.4K cycles at the
+        // end of every CTA.) Rows past Nk are not stored: the copy stops at
+        // the tensor's edge.
 #pragma unroll
         for (int which = part; which < 2; which += kRowWarpsB / 4) {   // 0: dV, 1: dK
             const uint32_t a = tmem + lane_base + (which ? C::cDK : C::cDV);
             const float mul = which ? scale : 1.f;
-            __nv_bfloat16* dst = (which ? dk : dv) + orow;
+            const uint32_t tile = sbase + (which ? C::kKOff : C::kVOff);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 32; ++cc) {                    // 32 head dims at a time
                 uint32_t v32[32];
                 if (have) {
                     ptx::tmem_ld32x32b_x32(a + cc * 32, v32);
@@ -649,18 +655,31 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v32[e] = 0u;
                 }
-                if (key < Nk) {
-                    uint32_t pw[16];
+                const uint32_t rbase = tile + (cc / 2) * C::kChunkBytes + r * 128;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pw[e] = pack_bf16x2(__uint_as_float(v32[2 * e]) * mul,
-                                            __uint_as_float(v32[2 * e + 1]) * mul);
-                    uint4* o4 = reinterpret_cast<uint4*>(dst + cc * 32);
+                for (int e = 0; e < 4; ++e) {                          // 16-byte pieces
+                    uint32_t pw[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o4[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+                    for (int f = 0; f < 4; ++f)
+                        pw[f] = pack_bf16x2(__uint_as_float(v32[8 * e + 2 * f]) * mul,
+                                            __uint_as_float(v32[8 * e + 2 * f + 1]) * mul);
+                    const int j = (cc % 2) * 4 + e;
+                    ptx::st_shared_v4(rbase + ((j ^ (r & 7)) << 4), pw[0], pw[1], pw[2], pw[3]);
                 }
             }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(1, 32 * kRowWarpsB);                   // every row warp
+        if (warp == 0 && lane == 0) {
+#pragma unroll
+            for (int which = 0; which < 2; ++which)
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_store_3d(which ? &tm_dk : &tm_dv,
+                                      sbase + (which ? C::kKOff : C::kVOff) + c * C::kChunkBytes,
+                                      c * 64, kb, bh);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_read_all();            // the tiles outlive the copies' reads
         }
     }
 
@@ -1038,8 +1057,9 @@ bwd_dq_convert_kernel(const float* __restrict__ ws_dq, __nv_bfloat16* __restrict
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,
-                         const CUtensorMap& tv64, cudaStream_t stream) {
+                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                         const CUtensorMap& tdv, const CUtensorMap& tk64, const CUtensorMap& tv64,
+                         cudaStream_t stream) {
     constexpr bool FQ = (D == 128) && ATTN_BWD_FUSED_DQ != 0;
     static int cfg_kv = -1, cfg_q = -1;
     cudaError_t e = set_smem(bwd_dkdv_kernel<D, FQ>, KVCfg<D, FQ>::kSmemBytes, &cfg_kv);
@@ -1059,8 +1079,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     dim3 g1((a.Nk + BT - 1) / BT, a.H, a.B);
     bwd_dkdv_kernel<D, FQ><<<g1, dkdv_threads<FQ>(), KVCfg<D, FQ>::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, a.ws_lse2, a.ws_dd, ws_dq, static_cast<__nv_bfloat16*>(a.dk),
-        static_cast<__nv_bfloat16*>(a.dv), a.H, a.Nq, a.Nk, Nq_pad, scale_log2, a.scale,
+        tq, tk, tv, tdo, tdk, tdv, a.ws_lse2, a.ws_dd, ws_dq, a.H, a.Nq, a.Nk, Nq_pad, scale_log2,
+        a.scale,
         a.mask_kind, a.window, a.seqlens_k, a.err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (FQ) {
@@ -1085,10 +1105,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensor
 bool bwd_fused_dq(int d) { return d == 128 && ATTN_BWD_FUSED_DQ != 0; }
 
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,
-                       const CUtensorMap& tv64, cudaStream_t stream) {
-    return a.d == 64 ? launch_bwd_d<64>(a, tq, tk, tv, tdo, tk64, tv64, stream)
-                     : launch_bwd_d<128>(a, tq, tk, tv, tdo, tk64, tv64, stream);
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const CUtensorMap& tk64, const CUtensorMap& tv64,
+                       cudaStream_t stream) {
+    return a.d == 64 ? launch_bwd_d<64>(a, tq, tk, tv, tdo, tdk, tdv, tk64, tv64, stream)
+                     : launch_bwd_d<128>(a, tq, tk, tv, tdo, tdk, tdv, tk64, tv64, stream);
 }
 
 }  // namespace attn

@@ -143,9 +143,12 @@ struct BwdArgs {
 // True when attn_bwd accumulates dQ inside the keys-outer kernel for head
 // dimension d (and so needs the FP32 dQ workspace).
 bool bwd_fused_dq(int d);
+// tdk, tdv: maps of dk and dv with the layout of tk and tv (the dK/dV
+// epilogue's stores)
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tk64,
-                       const CUtensorMap& tv64, cudaStream_t stream);
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const CUtensorMap& tk64, const CUtensorMap& tv64,
+                       cudaStream_t stream);
 cudaError_t launch_softmax_rows(const void* x, void* y, float* lse, long long rows, int n,
                                 bool bf16, cudaStream_t stream);
 cudaError_t launch_fill_empty(void* o, float* lse, long long rows, int d, bool bf16,
