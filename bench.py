@@ -53,7 +53,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # SHA-256 at capture time; reported as null when the source has changed.
 FWD_SHA = "dc3f63a62c8cfac140dcaeb3d158dbbdd03fd769809ab51675e7987628bf3cd4"
 DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
-BWD_SHA = "c47d5c0b04f877d8cb5b8dcbc7b72c99c5d4157365c91755eb893bdd8f751e83"
+BWD_SHA = "8dcdfba2ec4d76be16c5c2f1862f1022208f2f3def1d87dbc2304b3feb42e614"
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
     # launch at the full bench workload, 1-pass ncu capture; valid while the
@@ -74,8 +74,8 @@ NCU_TRAFFIC = {
                "bytes_per_launch": 2147542528 + 3053312 + 1072640,
                "workload": "decode_B1_H32_Nk131072_d128_bf16_splits64 (split and combine kernels)"},
     "backward": {"file": "bwd_sm103.cu", "sha256": BWD_SHA,
-                 "bytes_per_launch": (270547456 + 219994880) + (809643008 + 488216064) +
-                                     (268460544 + 86488064),
+                 "bytes_per_launch": (270548736 + 219377920) + (809734144 + 489436928) +
+                                     (268457728 + 86584064),
                  "workload": "prefill_B1_H64_N8192_d128_bf16 backward (prep, dK/dV/dQ and "
                              "dQ convert kernels)"},
     "softmax": {"file": "softmax.cu",
