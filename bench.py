@@ -53,7 +53,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # SHA-256 at capture time; reported as null when the source has changed.
 FWD_SHA = "610b407d8f30bdba053eec478d01ae79749a7ceaf71d5d405d09cf9b3f84dc4a"
 DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
-BWD_SHA = "8dcdfba2ec4d76be16c5c2f1862f1022208f2f3def1d87dbc2304b3feb42e614"
+BWD_SHA = "fdbb1b59f065fa898430ea6f21ebe4222e70637f063194ae96c1c755f5445251"
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel, one
     # launch at the full bench workload, 1-pass ncu capture; valid while the

@@ -28,7 +28,8 @@
 //                     dQ warps read dQ_u^T out and add it into the FP32
 //                     accumulator with red.global.add (one 128-byte line per
 //                     warp instruction). Five products per unit, none
-//                     recomputed.
+//                     recomputed. At the end dK and dV leave through the
+//                     CTA's K and V tiles by TMA stores.
 //   bwd_dq_convert_kernel  dQ = scale * accumulator, rounded to BF16.
 // d = 64 (and builds with ATTN_BWD_FUSED_DQ=0) keep dQ in its own pass:
 //   bwd_dq_kernel     queries outer: a CTA owns 128 queries; per unit of 64
