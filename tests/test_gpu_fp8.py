@@ -111,6 +111,9 @@ SHAPES = [
     (2, 2, 700, 700, W.MASK_CAUSAL, 0, None),
     (2, 3, 520, 900, W.MASK_WINDOW | W.MASK_PADDING, 200, (0, 900)),
     (1, 2, 77, 3000, W.MASK_PADDING, 0, (1, 3000)),
+    # causal CTAs walk their key blocks from the diagonal down over many
+    # blocks (up to 32 per CTA, past both rings' wrap-around)
+    (1, 1, 4096, 4096, W.MASK_CAUSAL, 0, None),
 ]
 
 

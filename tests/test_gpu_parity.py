@@ -349,6 +349,24 @@ def test_decode_bindings_check_output_shapes(cuda_lib):
             fn(q, k, k, o, lse=short_lse.contiguous()[:, :1], num_splits=4)
 
 
+@pytest.mark.parametrize("d,Nq,mk,sr", [
+    (64, 3000, W.MASK_CAUSAL, None),
+    (128, 3100, W.MASK_CAUSAL, None),
+    (128, 2600, W.MASK_CAUSAL | W.MASK_PADDING, (1, 2600)),
+])
+def test_fwd_causal_reversed_walk_long(cuda_lib, orc, d, Nq, mk, sr):
+    """Causal CTAs whose tile 1 sees the diagonal block more walk their key
+    blocks from the diagonal down (tile 0 starting one step later): rows of
+    up to 24 key blocks, both head dims (K/V rings of 5 + 4 and 3 + 2
+    slots, several wrap-arounds), a ragged last tile, and padded key
+    lengths that cut some CTAs' walk short, element by element against the
+    oracle."""
+    x = W.random_inputs(2, 2, Nq, Nq, d, seed=Nq + d, seqlen_range=sr)
+    o, lse = run_fwd(cuda_lib, x, mk)
+    ro, rl = oracle_fwd(orc, x, mk)
+    assert_close(o, lse, ro, rl, TOL_O_BF16, TOL_LSE, what="d%d Nq%d" % (d, Nq))
+
+
 # ------------------------------------------------ host-memory pipelined API
 @pytest.mark.parametrize("shape", [
     (2, 3, 300, 300, 128, W.MASK_CAUSAL, 0, None, 4),
