@@ -589,12 +589,17 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // peeled and each tile's Q had its own barrier, 1.108 -> 1.070 ms).
             // A causal tile 1 covers one block more than tile 0 (the
             // diagonal block of its own rows): walked from the last block
-            // down (rev), tile 0 starts one step later; otherwise (a window
-            // that clips neither tile) the same loop runs up to tile 0's last
-            // step, then one step of tile 1's.
+            // down (rev), tile 0 starts one step later; otherwise the same
+            // loop runs up to tile 0's last step, then one step of tile 1's.
+            // Under a sliding window tile 1 also starts one step later
+            // (late1: the window's lower edge is one block later for its
+            // rows), and its first S comes first in that step, as the slot
+            // release rule of early_s expects.
             const int h0 = R[0].hi, h1 = R[1].hi;
             const int off0 = R[0].lo - lo;          // tile 0's first step (1 when rev)
-            const bool uniform = !PAIR && (R[0].lo == lo || rev) && R[1].lo == lo &&
+            const int off1 = R[1].lo - lo;          // tile 1's first step (1 when late1)
+            const bool late1 = !rev && early_s == lo + 1 && R[0].lo == lo && h0 > lo + 1;
+            const bool uniform = !PAIR && (R[0].lo == lo || rev) && (R[1].lo == lo || late1) &&
                                  h1 == hi && (h0 == hi || h0 == hi - 1);
             if (uniform) {
                 // step 0, peeled: S_t once Q_t and the first K block have
@@ -639,6 +644,32 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     s_first = lo + 2;
                 }
+                if (late1 && ok) {
+                    // step 1, peeled: tile 1's first S, then tile 0's first
+                    // P V product and its next S
+                    constexpr int kst = 1 % NSK, vst = 0;
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + kst), (1 / NSK) & 1,
+                                                              abort_flag, err, kSiteKFull));
+                    if (ok)
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bQFull + 1), 0, abort_flag,
+                                                                  err, kSiteQFull));
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        if (leader) issue_s(1, kst);
+                        __syncwarp();
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull), 0, abort_flag,
+                                                                  err, kSitePFull));
+                    }
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        if (leader) {
+                            issue_pv(0, vst, true);
+                            issue_s(0, kst);                 // h0 > lo + 1 when late1
+                        }
+                        __syncwarp();
+                    }
+                    s_first = lo + 2;
+                }
                 for (int s = s_first; ok && s <= h0; ++s) {
                     const int i = s - lo;
                     const int kst = i % NSK;
@@ -648,7 +679,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (!ok) break;
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
-                        const int pi = i - 1 - (t == 0 ? off0 : 0);   // tile t's P hand-off index
+                        const int pi = i - 1 - (t == 0 ? off0 : off1);   // tile t's P hand-off index
                         ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + t), pi & 1,
                                                                   abort_flag, err, kSitePFull));
                         if (!ok) break;
@@ -671,12 +702,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bStep + i % NSK), (i / NSK) & 1,
                                                               abort_flag, err, kSiteKFull));
                     if (ok)
-                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + 1), (i - 1) & 1,
-                                                                  abort_flag, err, kSitePFull));
+                        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::bPFull + 1),
+                                                                  (i - 1 - off1) & 1, abort_flag,
+                                                                  err, kSitePFull));
                     if (ok) {
                         ptx::tc_fence_after();
                         if (leader) {
-                            issue_pv(1, (i + NSV - 1) % NSV, i == 1);
+                            issue_pv(1, (i + NSV - 1) % NSV, i - 1 - off1 == 0);
                             commit(C::bODone + 1);
                         }
                         __syncwarp();
