@@ -333,12 +333,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                      R[0].hi == hi - 1;
     if (rev) R[0] = Range{lo + 1, hi};
     auto blk = [&](int v) { return rev ? lo + hi - 1 - v : v; };
-    // Tile 1 starting inside tile 0's range, one or more blocks later (a
-    // sliding window): its first S product is issued at the start of that
-    // step, ahead of tile 0's P V product of the previous block, so that its
-    // softmax does not wait for tile 0's first one. That step's K and V
-    // blocks are then last read by tile 0's S product, and tile 0's softmax
-    // releases them (see the release rule below).
+    // Tile 1 starting inside tile 0's range, one block later (a sliding
+    // window; the straight-line schedule's late1 case below): its first S
+    // product is issued at the start of that step, ahead of tile 0's P V
+    // product of the previous block, so that its softmax does not wait for
+    // tile 0's first one. That step's K and V blocks are then last read by
+    // tile 0's S product, and tile 0's softmax releases them (see the
+    // release rule below).
     const int early_s = (!PAIR && R[1].lo > R[0].lo && R[1].lo < R[0].hi && R[1].lo < R[1].hi)
                             ? R[1].lo : -1;
     // This CTA's Q tiles, loaded into its own shared memory; completion is
@@ -723,19 +724,6 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // The step barrier (K_s and V_{s-1} landed) is waited right
                 // before the step's first MMA, and once per step in any case.
                 bool kv_ready = false;
-                if (s == early_s) {
-                    // S_1 = Q_1 K_s^T first: tile 1 has no earlier block
-                    ok = __all_sync(0xffffffffu, wait_bounded<PAIR>(bar(C::bStep + kst), kph,
-                                                                    abort_flag, err, kSiteKFull));
-                    if (ok)
-                        ok = __all_sync(0xffffffffu, wait_bounded<PAIR>(bar(C::bQFull + 1), 0,
-                                                                        abort_flag, err, kSiteQFull));
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    kv_ready = true;
-                    if (leader) issue_s(1, kst);
-                    __syncwarp();
-                }
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (s - 1 >= R[t].lo && s - 1 < R[t].hi) {
@@ -759,7 +747,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         __syncwarp();
                         ++pv_done[t];
                     }
-                    if (s < hi && s >= R[t].lo && s < R[t].hi && !(t == 1 && s == early_s)) {
+                    if (s < hi && s >= R[t].lo && s < R[t].hi) {
                         // S_t = Q_t K_s^T (the tile's first: once its Q has landed)
                         if (!kv_ready) {
                             ok = __all_sync(0xffffffffu,
