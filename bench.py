@@ -51,7 +51,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the source file of the kernel and its
 # SHA-256 at capture time; reported as null when the source has changed.
-FWD_SHA = "167e2b5bd53a621ed1b064566babc72e3a2d6b7d33dc474f40268ae1f1cf40d3"
+FWD_SHA = "a90cb2b22764f1bdc2d34a18a6895e271d9c4bb11e6627e2d1a858e49361d061"
 DECODE_SHA = "7662e21a7cbf9d910c984e96fe5bbcb4d5fb74d6a0723a8a014cf6588b014b54"
 BWD_SHA = "fdbb1b59f065fa898430ea6f21ebe4222e70637f063194ae96c1c755f5445251"
 NCU_TRAFFIC = {
@@ -59,16 +59,16 @@ NCU_TRAFFIC = {
     # launch at the full bench workload, 1-pass ncu capture; valid while the
     # kernel source is unchanged.
     "fwd_bf16": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                 "bytes_per_launch": 402934784 + 115970816,
+                 "bytes_per_launch": 402833152 + 114113792,
                  "workload": "prefill_B1_H64_N8192_d128_bf16"},
     "fwd_bf16_causal": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                        "bytes_per_launch": 402768128 + 113304576,
+                        "bytes_per_launch": 402730240 + 112965376,
                         "workload": "causal_B2_H32_N8192_d128_bf16"},
     "fwd_bf16_masked": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                        "bytes_per_launch": 243712256 + 109714432,
+                        "bytes_per_launch": 245462528 + 114034176,
                         "workload": "masked_B8_H16_N4096_d128_bf16_window1024_padded"},
     "fwd_e4m3": {"file": "fwd_sm103.cu", "sha256": FWD_SHA,
-                 "bytes_per_launch": 201462784 + 104351488,
+                 "bytes_per_launch": 201401088 + 102112256,
                  "workload": "prefill_B1_H64_N8192_d128_e4m3"},
     "decode": {"file": "decode.cu", "sha256": DECODE_SHA,
                "bytes_per_launch": 2147542528 + 3053312 + 1072640,

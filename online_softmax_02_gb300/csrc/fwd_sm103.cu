@@ -1021,12 +1021,17 @@ cudaError_t launch_d(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap&
     const int units = (a.Nq + C::kMmaM * NT - 1) / (C::kMmaM * NT);
     dim3 grid(units * C::kCtas, a.H, a.B);
     // Causal or windowed: longest units first within groups of heads whose
-    // K and V together take about 32 MiB (a quarter of L2).
+    // K and V together take about a quarter of L2 (32 MiB), or half of it
+    // (64 MiB) under a sliding window, where a CTA reads only a window's
+    // worth of K and V (masked B8 H16 4096^2: 0.1653 -> 0.1606 ms, the
+    // longest-first order balancing over twice the heads; causal B2 H32
+    // 8192^2 kept its time with half but re-read 45 MB of K and V).
     int group_heads = 0;
     if (a.mask_kind & (kMaskCausal | kMaskWindow)) {
         const long long nbh = static_cast<long long>(a.B) * a.H;
         const long long kv_head = 2LL * a.Nk * a.d * C::kElem;
-        const long long g = std::max(1LL, (32LL << 20) / std::max(kv_head, 1LL));
+        const long long budget = (a.mask_kind & kMaskWindow) ? (64LL << 20) : (32LL << 20);
+        const long long g = std::max(1LL, budget / std::max(kv_head, 1LL));
         group_heads = static_cast<int>(std::min(g, nbh));
         // the kernel computes this order in 32-bit arithmetic
         if (static_cast<long long>(grid.x) * grid.y * grid.z > INT_MAX) group_heads = 0;
